@@ -1,0 +1,281 @@
+"""Plain, slow fp64 CPU oracle for the forward pass of one sparse MoE layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only the test suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it.  It shares no code, table, constant
+or helper with the CUDA library; both sides take their inputs from the
+seeded generator in ``sparse_mixture_experts_51_b300.workloads``, which holds
+none of the method's arithmetic.
+
+Everything is evaluated in float64 from the values stored in the input
+arrays (bf16 values widened exactly).  Each function names the passage of
+the source pages it restates.  The pages are cited by title and section:
+
+  [P1] "Mixture-of-Experts Sparse Model Scaling" (glossary page), sections
+       "Mathematical Formulation", "Advanced Theory & Extensions", and the
+       "Practical Labs" appendix (Lab 1 top-k router, Lab 3 capacity).
+  [P2] "Mixture-of-experts Models" (book chapter), Level 2 "Router scores
+       become a sparse dispatch decision", "Top-k selection has ties",
+       "Capacity limits make dispatch observable" (Figure 44.4).
+  [P3] "Scaling Capacity via Sparse Mixture of Experts (MoE) Architectures",
+       the SimpleRouter listing.
+  [P4] "LLM part 09: Sparse Mixture-of-Experts (MoE)", section 1 (output
+       equation), section 2 (noisy top-k gating), section 3 (capacity).
+  [P5] "3D mixture-of-experts routing lab", the "Capacity" card.
+
+Readings taken where the pages are silent or disagree:
+  * gates are renormalised over the selected experts ([P1] Lab 1, [P2]
+    Level 2, [P3] SimpleRouter, [P4] s2 all do so; [P1]'s displayed
+    equation does not, and is the minority reading);
+  * ties in the top-k order go to the lower expert index;
+  * capacity C = ceil(cf * T * k / E) in float64 ([P5] capacity card);
+  * dispatch priority is rank-major: every token's first choice, in token
+    order, before any second choice; an assignment is kept iff fewer than C
+    earlier assignments went to the same expert ([P1] Lab 3 generalised);
+  * a dropped assignment contributes nothing; the gates of the survivors
+    are NOT renormalised again; the residual carries the token
+    ([P1] "Advanced Theory", [P4] s3);
+  * GELU is the exact erf form; SwiGLU is silu(x W1^T) * (x W3^T); the
+    noise branch has no bias; softplus(z) = max(z,0) + log1p(exp(-|z|));
+    SwiGLU experts take no b1 (b2 is optional for both forms).
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+try:
+    from scipy.special import erf as _erf
+except ImportError:  # pragma: no cover - scipy is present in the image
+    _erf = np.vectorize(math.erf, otypes=[np.float64])
+
+GELU = 0
+SWIGLU = 1
+
+
+# --------------------------------------------------------------------------
+# routing
+# --------------------------------------------------------------------------
+
+def softplus(z: np.ndarray) -> np.ndarray:
+    """softplus(z) = ln(1 + e^z), written in the overflow-free form."""
+    z = np.asarray(z, dtype=np.float64)
+    return np.maximum(z, 0.0) + np.log1p(np.exp(-np.abs(z)))
+
+
+def logits(x, W_g, b_g=None, W_noise=None, eps=None) -> np.ndarray:
+    """Router logits H[t,e] ([P4] s2 noisy top-k gating; [P1] "Mathematical
+    Formulation": g_i(x) is a linear transform of x; [P3] SimpleRouter's
+    nn.Linear carries a bias).
+
+        H = x W_g + b_g + eps * softplus(x W_noise)
+
+    x [T,d], W_g [d,E], b_g [E] or None, W_noise [d,E] or None, eps [T,E] or None.
+    The noise term is present only when both W_noise and eps are given.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    H = x @ np.asarray(W_g, dtype=np.float64)
+    if b_g is not None:
+        H = H + np.asarray(b_g, dtype=np.float64)[None, :]
+    if W_noise is not None and eps is not None:
+        H = H + np.asarray(eps, dtype=np.float64) * softplus(x @ np.asarray(W_noise, dtype=np.float64))
+    return H
+
+
+def topk(H: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, largest first ([P4] s2 TopK;
+    [P1] Lab 1 ranks experts by descending probability; softmax is monotone
+    so ranking logits ranks probabilities).  Equal logits go to the lower
+    expert index: a stable sort of -H keeps index order among equals.
+    Returns int64 [T,k].
+    """
+    H = np.asarray(H, dtype=np.float64)
+    order = np.argsort(-H, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def gates(H: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Gate weights w[t,r] = softmax over the k selected logits ([P4] s2:
+    G = Softmax(TopK(H)); equal to the renormalised top-k probabilities of
+    [P1] Lab 1 and [P2] Level 2).  Shifted by the largest selected logit.
+    """
+    sel = np.take_along_axis(np.asarray(H, dtype=np.float64), idx, axis=1)
+    z = np.exp(sel - sel.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def capacity(T: int, k: int, E: int, capacity_factor: float) -> int:
+    """Expert capacity C = ceil(factor * tokens * k / experts) ([P5] Capacity
+    card; [P4] s3 gives the k=1 form)."""
+    return int(math.ceil(float(capacity_factor) * float(T) * float(k) / float(E)))
+
+
+def dispatch(idx: np.ndarray, E: int, C: int) -> dict:
+    """Capacity-limited first-come dispatch ([P1] Lab 3; [P2] "Capacity limits
+    make dispatch observable").
+
+    Assignments are visited in priority order: rank 0 of every token in token
+    order, then rank 1, and so on.  An assignment takes the next slot of its
+    expert while the expert has fewer than C; otherwise it is dropped.
+
+    Returns dict with
+      pos     int64 [T,k]  slot within the expert's segment, -1 if dropped
+      load    int64 [E]    assignments requested per expert (before the cap)
+      counts  int64 [E]    kept assignments per expert = min(load, C)
+      offsets int64 [E+1]  exclusive prefix sum of counts (segment starts)
+      dropped int          number of dropped assignments
+    """
+    idx = np.asarray(idx, dtype=np.int64)
+    T, k = idx.shape
+    load = np.zeros(E, dtype=np.int64)
+    pos = np.full((T, k), -1, dtype=np.int64)
+    dropped = 0
+    for r in range(k):
+        for t in range(T):
+            e = int(idx[t, r])
+            slot = int(load[e])
+            load[e] += 1
+            if slot < C:
+                pos[t, r] = slot
+            else:
+                dropped += 1
+    counts = np.minimum(load, C)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + counts[e]
+    return dict(pos=pos, load=load, counts=counts, offsets=offsets, dropped=int(dropped))
+
+
+# --------------------------------------------------------------------------
+# experts
+# --------------------------------------------------------------------------
+
+def gelu(a: np.ndarray) -> np.ndarray:
+    """Exact GELU: a * Phi(a) = a * (1 + erf(a / sqrt 2)) / 2 (erf from scipy)."""
+    a = np.asarray(a, dtype=np.float64)
+    return a * 0.5 * (1.0 + _erf(a / math.sqrt(2.0)))
+
+
+def silu(a: np.ndarray) -> np.ndarray:
+    """SiLU: a * sigmoid(a)."""
+    a = np.asarray(a, dtype=np.float64)
+    return a / (1.0 + np.exp(-a))
+
+
+def expert(xr: np.ndarray, e: int, act: int, W1, W3, W2, b1=None, b2=None) -> np.ndarray:
+    """Output of expert e on rows xr [n,d] ([P1] "Core Concepts": each expert
+    is a feed-forward network with the architecture of the dense FFN it
+    replaces; the GELU and SwiGLU forms are the two the layer supports).
+
+      GELU   : y = gelu(xr W1[e]^T + b1[e]) W2[e]^T + b2[e]
+      SwiGLU : y = (silu(xr W1[e]^T) * (xr W3[e]^T)) W2[e]^T (+ b2[e])
+
+    Weights are in nn.Linear layout: W1, W3 [E,F,d], W2 [E,d,F].
+    """
+    xr = np.asarray(xr, dtype=np.float64)
+    w1 = np.asarray(W1[e], dtype=np.float64)
+    a = xr @ w1.T
+    if act == GELU:
+        if b1 is not None:
+            a = a + np.asarray(b1[e], dtype=np.float64)[None, :]
+        h = gelu(a)
+    elif act == SWIGLU:
+        w3 = np.asarray(W3[e], dtype=np.float64)
+        h = silu(a) * (xr @ w3.T)
+    else:
+        raise ValueError(f"unknown activation {act}")
+    y = h @ np.asarray(W2[e], dtype=np.float64).T
+    if b2 is not None:
+        y = y + np.asarray(b2[e], dtype=np.float64)[None, :]
+    return y
+
+
+# --------------------------------------------------------------------------
+# whole layer
+# --------------------------------------------------------------------------
+
+def combine(x, idx, w, pos, expert_out, residual=True, tokens=None) -> dict:
+    """Weighted combination y = sum_i G(x)_i E_i(x) over the kept assignments
+    ([P4] s1; [P1] "Mathematical Formulation"; [P1] Lab 1 accumulates
+    weight * expert output per token), plus the residual that carries a
+    dropped token through unchanged ([P1] "Advanced Theory"; [P4] s3).
+
+    expert_out[(t, r)] holds E_{idx[t,r]}(x_t) for every kept (t, r) of the
+    tokens evaluated.  Ranks are summed in order 0..k-1.
+    Returns moe [n,d] (the weighted expert sum) and out = x + moe for the
+    rows in ``tokens`` (all tokens when None).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, k = idx.shape
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    moe = np.zeros((len(toks), x.shape[1]), dtype=np.float64)
+    for i, t in enumerate(toks):
+        for r in range(k):
+            if pos[t, r] >= 0:
+                moe[i] += w[t, r] * expert_out[(int(t), r)]
+    out = x[toks] + moe if residual else moe.copy()
+    return dict(moe=moe, out=out)
+
+
+def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
+            b_g=None, W_noise=None, eps=None, capacity_factor: Optional[float] = None,
+            C: Optional[int] = None, tokens=None, idx_override=None) -> dict:
+    """Forward pass of one sparse MoE layer, step by step.
+
+    1 logits ([P4] s2) -> 2 top-k ([P4] s2) -> 3 gates ([P4] s2) ->
+    4 capacity ([P5]) -> 5 dispatch ([P1] Lab 3) -> 6 experts on the kept
+    assignments -> 7 combine + residual ([P4] s1, s3).
+
+    ``tokens``: evaluate experts and combine only for these token ids
+    (routing and dispatch always cover the whole batch, since capacity
+    couples all tokens).  ``idx_override``: dispatch/combine a given top-k
+    index table instead of the oracle's own (used to check the later stages
+    on another router's decisions); gates still come from the oracle's H.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape
+    E = np.asarray(W_g).shape[1]
+    H = logits(x, W_g, b_g, W_noise, eps)
+    idx = topk(H, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
+    w = gates(H, idx)
+    if C is None:
+        C = capacity(T, k, E, capacity_factor)
+    disp = dispatch(idx, E, C)
+    pos = disp["pos"]
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    per_expert = [[] for _ in range(E)]
+    for t in toks:
+        for r in range(k):
+            if pos[t, r] >= 0:
+                per_expert[int(idx[t, r])].append((int(t), r))
+    expert_out = {}
+    for e in range(E):
+        pairs = per_expert[e]
+        if not pairs:
+            continue
+        rows = np.stack([x[t] for t, _ in pairs])
+        y = expert(rows, e, act, W1, W3, W2, b1, b2)
+        for i, p in enumerate(pairs):
+            expert_out[p] = y[i]
+    comb = combine(x, idx, w, pos, expert_out, residual=True, tokens=toks)
+    return dict(H=H, idx=idx, w=w, C=C, tokens=toks, **disp, **comb)
+
+
+def near_ties(H: np.ndarray, k: int, thresh: float = 1e-4) -> dict:
+    """Near-tie report: tokens whose k-th and (k+1)-th largest logits differ
+    by less than ``thresh``, and tokens with any adjacent gap under ``thresh``
+    among their k+1 largest logits (a swap inside the top k changes the rank
+    order, hence the dispatch priority)."""
+    H = np.asarray(H, dtype=np.float64)
+    E = H.shape[1]
+    s = -np.sort(-H, axis=1)
+    boundary = np.zeros(H.shape[0], dtype=bool)
+    if k < E:
+        boundary = (s[:, k - 1] - s[:, k]) < thresh
+    m = min(k + 1, E)
+    inner = np.zeros(H.shape[0], dtype=bool)
+    for j in range(m - 1):
+        inner |= (s[:, j] - s[:, j + 1]) < thresh
+    return dict(boundary=np.nonzero(boundary)[0], any_adjacent=np.nonzero(inner)[0])

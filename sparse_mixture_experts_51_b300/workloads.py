@@ -1,0 +1,148 @@
+"""Seeded synthetic workloads for the sparse MoE layer forward.
+
+This module only draws random numbers and builds tensors of the right
+shapes and dtypes.  It holds none of the layer's arithmetic (no routing,
+no dispatch, no expert math), so both the CUDA path and the CPU oracle can
+take their inputs from it without sharing any of the method.
+
+Shapes follow the five layer configurations this library is measured on:
+
+  tiny_fp32       T=64    d=32   E=4  k=2 GELU   F=64    cf=1.25  fp32
+  bf16_t4096      T=4096  d=1024 E=8  k=2 SwiGLU F=4096  cf=1.25  bf16
+  mixtral_t16384  T=16384 d=4096 E=8  k=2 SwiGLU F=14336 no-drop  bf16
+  switch_top1     T=32768 d=768  E=64 k=1 GELU   F=3072  cf=1.0   bf16,
+                  Zipf router bias and noisy gating
+  decode_t128     T=128   d=2048 E=64 k=6 SwiGLU F=1408  cf=2.0   bf16
+
+Value recipe (all draws fp32 standard normal from one CPU torch.Generator
+seeded per workload, scaled, then cast to the storage dtype):
+  x ~ N(0,1); W_g ~ N(0, 1/d); W1, W3 ~ N(0, 1/d); W2 ~ N(0, 1/F)
+  (tiny_fp32 takes "N(0, 1/d)" literally for every weight, W2 included);
+  biases zero (tiny_fp32 carries explicit zero b1/b2; the others have none);
+  switch_top1: b_g[e] = 2*ln(1/(e+1)), W_noise ~ N(0, 1/d), eps ~ N(0,1)[T,E].
+The draw order is fixed: x, W_g, W_noise, eps, W1, W3, W2.
+
+Layouts (row-major, nn.Linear style, K contiguous):
+  x [T,d]; W_g [d,E] fp32; b_g [E] fp32; W_noise [d,E] fp32; eps [T,E] fp32;
+  W1, W3 [E,F,d]; W2 [E,d,F]; b1 [E,F] fp32; b2 [E,d] fp32.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import torch
+
+ACT_GELU = 0
+ACT_SWIGLU = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    T: int
+    d: int
+    E: int
+    k: int
+    F: int
+    act: int                 # ACT_GELU or ACT_SWIGLU
+    capacity_factor: float
+    dtype: torch.dtype       # storage/compute dtype of x, expert weights, out
+    seed: int
+    noisy: bool = False      # noisy gating with supplied eps and W_noise
+    zipf_bias: bool = False  # router bias b_e = 2 ln(1/(e+1))
+    expert_bias: bool = False  # explicit (zero) b1/b2 tensors
+    weight_std_literal_d: bool = False  # every weight ~N(0,1/d)
+
+    @property
+    def dtype_name(self) -> str:
+        return {torch.float32: "f32", torch.bfloat16: "bf16"}[self.dtype]
+
+    def scaled(self, T: int, seed: Optional[int] = None) -> "Workload":
+        """Same layer with a different token count (used for small parity cases)."""
+        return dataclasses.replace(self, T=T, seed=self.seed if seed is None else seed,
+                                   name=f"{self.name}@T{T}")
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload("tiny_fp32", T=64, d=32, E=4, k=2, F=64, act=ACT_GELU,
+                          capacity_factor=1.25, dtype=torch.float32, seed=0,
+                          expert_bias=True, weight_std_literal_d=True),
+    "bf16_t4096": Workload("bf16_t4096", T=4096, d=1024, E=8, k=2, F=4096, act=ACT_SWIGLU,
+                           capacity_factor=1.25, dtype=torch.bfloat16, seed=1),
+    # no-drop: capacity factor E/k makes C = T
+    "mixtral_t16384": Workload("mixtral_t16384", T=16384, d=4096, E=8, k=2, F=14336,
+                               act=ACT_SWIGLU, capacity_factor=4.0, dtype=torch.bfloat16,
+                               seed=3),
+    "switch_top1": Workload("switch_top1", T=32768, d=768, E=64, k=1, F=3072, act=ACT_GELU,
+                            capacity_factor=1.0, dtype=torch.bfloat16, seed=4,
+                            noisy=True, zipf_bias=True),
+    "decode_t128": Workload("decode_t128", T=128, d=2048, E=64, k=6, F=1408, act=ACT_SWIGLU,
+                            capacity_factor=2.0, dtype=torch.bfloat16, seed=5),
+}
+ORDER = ["tiny_fp32", "bf16_t4096", "mixtral_t16384", "switch_top1", "decode_t128"]
+
+
+def _normal(g: torch.Generator, shape, std: float) -> torch.Tensor:
+    t = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t
+
+
+def make_inputs(w: Workload) -> dict:
+    """Draw every input tensor of workload ``w`` on the CPU.
+
+    Returns a dict of CPU tensors: x, W_g, b_g (or None), W_noise (or None),
+    eps (or None), W1, W3 (or None), W2, b1 (or None), b2 (or None).
+    Expert weights and x are in ``w.dtype``; router tensors are fp32.
+    """
+    g = torch.Generator().manual_seed(w.seed)
+    T, d, E, F = w.T, w.d, w.E, w.F
+    std_d = 1.0 / math.sqrt(d)
+    std_f = std_d if w.weight_std_literal_d else 1.0 / math.sqrt(F)
+    x = _normal(g, (T, d), 1.0)
+    W_g = _normal(g, (d, E), std_d)
+    b_g = None
+    if w.zipf_bias:
+        b_g = torch.tensor([2.0 * math.log(1.0 / (e + 1)) for e in range(E)], dtype=torch.float32)
+    W_noise = eps = None
+    if w.noisy:
+        W_noise = _normal(g, (d, E), std_d)
+        eps = _normal(g, (T, E), 1.0)
+    W1 = _normal(g, (E, F, d), std_d)
+    W3 = _normal(g, (E, F, d), std_d) if w.act == ACT_SWIGLU else None
+    W2 = _normal(g, (E, d, F), std_f)
+    b1 = b2 = None
+    if w.expert_bias:
+        b1 = torch.zeros(E, F, dtype=torch.float32)
+        b2 = torch.zeros(E, d, dtype=torch.float32)
+    cast = (lambda t: t) if w.dtype == torch.float32 else (lambda t: t.to(w.dtype))
+    out = dict(x=cast(x), W_g=W_g, b_g=b_g, W_noise=W_noise, eps=eps,
+               W1=cast(W1), W3=None if W3 is None else cast(W3), W2=cast(W2),
+               b1=b1, b2=b2)
+    return out
+
+
+def make_tokens(w: Workload, seed: int) -> tuple:
+    """A fresh token batch (and noise, when the workload is noisy) for the same layer.
+
+    Used by timing loops that stream new inputs each step; weights are not redrawn.
+    """
+    g = torch.Generator().manual_seed(seed)
+    x = _normal(g, (w.T, w.d), 1.0)
+    eps = _normal(g, (w.T, w.E), 1.0) if w.noisy else None
+    if w.dtype != torch.float32:
+        x = x.to(w.dtype)
+    return x, eps
+
+
+def as_f64_numpy(t: Optional[torch.Tensor]):
+    """Widen a stored tensor (fp32 or bf16) to a float64 numpy array, exactly."""
+    if t is None:
+        return None
+    return t.detach().to("cpu").to(torch.float64).numpy()

@@ -1,0 +1,341 @@
+"""Pins for the fp64 oracle: each test checks it against something other than
+itself -- values the pages print, closed forms, special cases that reduce to
+a library routine, and brute force on tiny inputs.  CPU only."""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+from sparse_mixture_experts_51_b300 import workloads as W
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_worked_gating_example(golden_dir):
+    """Mixture-of-experts Models, Level 2: the printed top-two example."""
+    g = _load(golden_dir, "gating_example.json")
+    H = np.array([g["scores"]])
+    # the scores reach the oracle through its logits step (x = 1, W_g = scores)
+    H_from_logits = O.logits(np.ones((1, 1)), np.array([g["scores"]]))
+    np.testing.assert_array_equal(H_from_logits, H)
+    # printed softmax weights (3 decimals), independent of the oracle's gates()
+    p = torch.softmax(torch.tensor(H, dtype=torch.float64), dim=1).numpy()[0]
+    np.testing.assert_allclose(np.round(p, 3), g["printed_router_weights"], atol=0)
+    idx = O.topk(H, g["top_k"])[0]
+    assert sorted(idx.tolist()) == sorted(g["printed_experts_ascending"])
+    # the page prints ascending-weight order; the oracle returns largest first
+    assert idx.tolist() == list(reversed(g["printed_experts_ascending"]))
+    w = O.gates(H, O.topk(H, g["top_k"]))[0]
+    np.testing.assert_allclose(np.round(w[::-1], 3), g["printed_renormalised_ascending"], atol=0)
+    assert abs(w[0] - 0.64566) < 1e-5 and abs(w[1] - 0.35434) < 1e-5
+
+
+def test_worked_capacity_example(golden_dir):
+    """Mixture-of-experts Models, Level 2: loads and overflow printed for C=2."""
+    g = _load(golden_dir, "capacity_example.json")
+    idx = np.array(g["assignments"])[:, None]
+    d = O.dispatch(idx, g["n_experts"], g["capacity"])
+    assert d["load"].tolist() == g["printed_loads"]
+    assert np.maximum(d["load"] - g["capacity"], 0).tolist() == g["printed_overflow"]
+    assert d["dropped"] == sum(g["printed_overflow"])
+    # first come, first served (Lab 3): the third request for expert 0 is dropped
+    assert d["pos"][:, 0].tolist() == [0, 1, -1, 0, 1, 0, 0, 1]
+    assert d["counts"].tolist() == [2, 2, 1, 2]
+    assert d["offsets"].tolist() == [0, 2, 4, 5, 7]
+
+
+def test_capacities_of_the_five_layers(golden_dir):
+    g = _load(golden_dir, "configs.json")
+    for name, C in g["capacities"].items():
+        w = W.WORKLOADS[name]
+        assert O.capacity(w.T, w.k, w.E, w.capacity_factor) == C, name
+    # no-drop layer: C equals T
+    w = W.WORKLOADS["mixtral_t16384"]
+    assert O.capacity(w.T, w.k, w.E, w.capacity_factor) == w.T
+
+
+# ---------------------------------------------------------------- brute force
+
+def _brute_topk(H, k):
+    """rank(e) = #{e' : H[e'] > H[e] or (H[e'] == H[e] and e' < e)}; chosen iff rank < k."""
+    T, E = H.shape
+    out = np.zeros((T, k), dtype=np.int64)
+    for t in range(T):
+        for e in range(E):
+            rank = sum(1 for e2 in range(E) if H[t, e2] > H[t, e] or (H[t, e2] == H[t, e] and e2 < e))
+            if rank < k:
+                out[t, rank] = e
+    return out
+
+
+def _brute_dispatch(idx, E, C):
+    """pos(t,r) = #{(t',r') earlier in priority with the same expert}, O((Tk)^2)."""
+    T, k = idx.shape
+    order = [(r, t) for r in range(k) for t in range(T)]
+    pos = np.full((T, k), -1, dtype=np.int64)
+    load = [0] * E
+    for j, (r, t) in enumerate(order):
+        e = idx[t, r]
+        earlier = sum(1 for (r2, t2) in order[:j] if idx[t2, r2] == e)
+        load[e] += 1
+        if earlier < C:
+            pos[t, r] = earlier
+    return pos, np.array(load)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_brute_force_with_ties(seed):
+    rng = np.random.default_rng(seed)
+    T, E = 40, 7
+    # small integers force many exact ties
+    H = rng.integers(-3, 4, size=(T, E)).astype(np.float64)
+    for k in (1, 2, 3, E):
+        np.testing.assert_array_equal(O.topk(H, k), _brute_topk(H, k))
+
+
+def test_tie_goes_to_lower_index_through_logits():
+    # duplicated router columns give exactly equal logits (integer-valued, exact sums)
+    x = np.array([[1.0, 2.0, -1.0], [0.0, 1.0, 3.0]])
+    col = np.array([1.0, -2.0, 4.0])
+    W_g = np.stack([col * 0, col, col, col * -1], axis=1)  # experts 1 and 2 identical
+    H = O.logits(x, W_g)
+    assert H[0, 1] == H[0, 2] and H[1, 1] == H[1, 2]
+    idx = O.topk(H, 2)
+    assert idx[1].tolist() == [1, 2]  # H[1] = [0, 10, 10, -10]: tie 1 vs 2 -> 1 first
+    assert 1 in idx[0].tolist() or 0 in idx[0].tolist()
+
+
+@pytest.mark.parametrize("seed,T,E,k,C", [(0, 9, 3, 2, 4), (1, 12, 4, 3, 5), (2, 7, 5, 1, 1),
+                                          (3, 15, 4, 2, 3), (4, 6, 6, 6, 2), (5, 11, 2, 2, 100)])
+def test_dispatch_brute_force(seed, T, E, k, C):
+    rng = np.random.default_rng(seed)
+    # distinct experts per token, like a real top-k table
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    d = O.dispatch(idx, E, C)
+    pos, load = _brute_dispatch(idx, E, C)
+    np.testing.assert_array_equal(d["pos"], pos)
+    np.testing.assert_array_equal(d["load"], load)
+    assert d["dropped"] == int(np.maximum(load - C, 0).sum())
+    assert (d["counts"] <= C).all()
+    assert int(d["counts"].sum()) + d["dropped"] == T * k
+    # slots of each expert are exactly 0..counts-1
+    for e in range(E):
+        slots = sorted(d["pos"][(idx == e) & (d["pos"] >= 0)].tolist())
+        assert slots == list(range(int(d["counts"][e])))
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("seed", range(4))
+def test_gates_equal_renormalised_softmax(seed):
+    """softmax over the selected logits (LLM part 09 s2) equals the renormalised
+    top-k of the full softmax (Lab 1, Level 2, SimpleRouter)."""
+    rng = np.random.default_rng(seed)
+    H = rng.normal(size=(50, 9)) * 3
+    for k in (1, 2, 4, 9):
+        idx = O.topk(H, k)
+        w = O.gates(H, idx)
+        p = torch.softmax(torch.tensor(H), dim=1).numpy()
+        sel = np.take_along_axis(p, idx, axis=1)
+        np.testing.assert_allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-13)
+        assert (np.diff(w, axis=1) <= 1e-15).all()  # largest first
+    # top-1 gate is exactly 1
+    assert (O.gates(H, O.topk(H, 1)) == 1.0).all()
+
+
+def test_activation_functions_match_torch():
+    a = np.linspace(-9, 9, 2001)
+    ta = torch.tensor(a)
+    np.testing.assert_allclose(O.gelu(a), torch.nn.functional.gelu(ta).numpy(), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(O.silu(a), torch.nn.functional.silu(ta).numpy(), rtol=1e-14, atol=1e-15)
+    z = np.linspace(-40, 40, 2001)
+    np.testing.assert_allclose(O.softplus(z), torch.nn.functional.softplus(torch.tensor(z), threshold=1e9).numpy(),
+                               rtol=1e-14, atol=1e-300)
+
+
+def test_noise_term_closed_forms():
+    rng = np.random.default_rng(7)
+    T, d, E = 5, 4, 3
+    x = rng.normal(size=(T, d))
+    W_g = rng.normal(size=(d, E))
+    b_g = rng.normal(size=E)
+    eps = rng.normal(size=(T, E))
+    base = x @ W_g + b_g
+    # W_noise = 0 -> softplus(0) = ln 2
+    H = O.logits(x, W_g, b_g, np.zeros((d, E)), eps)
+    np.testing.assert_allclose(H, base + eps * math.log(2.0), rtol=1e-14, atol=1e-14)
+    # eps = 0 -> noiseless
+    Wn = rng.normal(size=(d, E))
+    np.testing.assert_allclose(O.logits(x, W_g, b_g, Wn, np.zeros((T, E))), base, rtol=0, atol=0)
+    # one scalar entry by hand
+    t, e = 2, 1
+    z = sum(x[t, j] * Wn[j, e] for j in range(d))
+    want = sum(x[t, j] * W_g[j, e] for j in range(d)) + b_g[e] + eps[t, e] * math.log1p(math.exp(z))
+    assert abs(O.logits(x, W_g, b_g, Wn, eps)[t, e] - want) < 1e-12
+
+
+def _loop_expert(xrow, e, act, W1, W3, W2, b1, b2):
+    """Pure-Python per-element expert (nn.Linear layout: out_f = sum_j x_j W[f, j])."""
+    F, d = W1.shape[1], W1.shape[2]
+    h = []
+    for f in range(F):
+        a = sum(xrow[j] * W1[e, f, j] for j in range(d))
+        if act == O.GELU:
+            a += 0.0 if b1 is None else b1[e, f]
+            h.append(a * 0.5 * (1 + math.erf(a / math.sqrt(2))))
+        else:
+            u = sum(xrow[j] * W3[e, f, j] for j in range(d))
+            h.append(a / (1 + math.exp(-a)) * u)
+    return np.array([sum(h[f] * W2[e, i, f] for f in range(F)) + (0.0 if b2 is None else b2[e, i])
+                     for i in range(d)])
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_expert_matches_elementwise_loops(act):
+    rng = np.random.default_rng(11)
+    E, d, F = 3, 5, 7  # non-square so a transposed operand cannot pass
+    W1 = rng.normal(size=(E, F, d))
+    W3 = rng.normal(size=(E, F, d))
+    W2 = rng.normal(size=(E, d, F))
+    b1 = rng.normal(size=(E, F)) if act == O.GELU else None
+    b2 = rng.normal(size=(E, d))
+    xr = rng.normal(size=(4, d))
+    for e in range(E):
+        y = O.expert(xr, e, act, W1, W3, W2, b1, b2)
+        for i in range(4):
+            np.testing.assert_allclose(y[i], _loop_expert(xr[i], e, act, W1, W3, W2, b1, b2), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- layer-level special cases
+
+def _tiny_layer(seed, T=24, d=6, E=4, F=5, act=O.GELU, bias=True):
+    rng = np.random.default_rng(seed)
+    return dict(x=rng.normal(size=(T, d)), W_g=rng.normal(size=(d, E)),
+                b_g=rng.normal(size=E) if bias else None,
+                W1=rng.normal(size=(E, F, d)) / math.sqrt(d), W3=rng.normal(size=(E, F, d)) / math.sqrt(d),
+                W2=rng.normal(size=(E, d, F)) / math.sqrt(F),
+                b1=rng.normal(size=(E, F)) if (bias and act == O.GELU) else None,
+                b2=rng.normal(size=(E, d)) if bias else None)
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_k_equals_E_is_dense_softmax_mixture(act):
+    """With k = E and C >= T every expert sees every token: the layer is the
+    dense softmax-weighted mixture of the 'Mathematical Formulation' with k = N."""
+    L = _tiny_layer(3, act=act)
+    T, E = L["x"].shape[0], L["W_g"].shape[1]
+    res = O.forward(L["x"], L["W_g"], E, act, L["W1"], L["W2"], L["W3"], L["b1"], L["b2"],
+                    b_g=L["b_g"], C=T)
+    assert res["dropped"] == 0
+    # dense form in torch fp64: softmax over all experts, every expert on every token
+    x = torch.tensor(L["x"])
+    p = torch.softmax(x @ torch.tensor(L["W_g"]) + torch.tensor(L["b_g"]), dim=1)
+    moe = torch.zeros_like(x)
+    for e in range(E):
+        a = x @ torch.tensor(L["W1"][e]).T
+        if act == O.GELU:
+            h = torch.nn.functional.gelu(a + torch.tensor(L["b1"][e]))
+        else:
+            h = torch.nn.functional.silu(a) * (x @ torch.tensor(L["W3"][e]).T)
+        y = h @ torch.tensor(L["W2"][e]).T + torch.tensor(L["b2"][e])
+        moe += p[:, e:e + 1] * y
+    np.testing.assert_allclose(res["moe"], moe.numpy(), rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(res["out"], (x + moe).numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_k1_is_argmax_expert_with_unit_gate():
+    L = _tiny_layer(4, act=O.SWIGLU)
+    T = L["x"].shape[0]
+    res = O.forward(L["x"], L["W_g"], 1, O.SWIGLU, L["W1"], L["W2"], L["W3"], None, L["b2"], b_g=L["b_g"], C=T)
+    H = L["x"] @ L["W_g"] + L["b_g"]
+    for t in range(T):
+        e = int(np.argmax(H[t]))
+        assert res["idx"][t, 0] == e and res["w"][t, 0] == 1.0
+        y = O.expert(L["x"][t:t + 1], e, O.SWIGLU, L["W1"], L["W3"], L["W2"], None, L["b2"])[0]
+        np.testing.assert_allclose(res["moe"][t], y, rtol=1e-13, atol=1e-14)
+
+
+def test_dropped_tokens_pass_through_and_gates_are_not_renormalised():
+    L = _tiny_layer(5, T=30)
+    k, C = 2, 3
+    res = O.forward(L["x"], L["W_g"], k, O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"], b_g=L["b_g"], C=C)
+    assert res["dropped"] > 0
+    pos, w, idx = res["pos"], res["w"], res["idx"]
+    for t in range(30):
+        kept = [r for r in range(k) if pos[t, r] >= 0]
+        if not kept:
+            np.testing.assert_array_equal(res["out"][t], L["x"][t])
+            assert not res["moe"][t].any()
+        want = np.zeros(L["x"].shape[1])
+        for r in kept:
+            want += w[t, r] * O.expert(L["x"][t:t + 1], int(idx[t, r]), O.GELU, L["W1"], None, L["W2"], L["b1"], L["b2"])[0]
+        np.testing.assert_allclose(res["moe"][t], want, rtol=1e-12, atol=1e-13)
+
+
+def test_token_subset_matches_full_evaluation():
+    L = _tiny_layer(6, T=40)
+    full = O.forward(L["x"], L["W_g"], 2, O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"], b_g=L["b_g"], C=14)
+    sub = [0, 7, 13, 39]
+    part = O.forward(L["x"], L["W_g"], 2, O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"], b_g=L["b_g"], C=14, tokens=sub)
+    np.testing.assert_allclose(part["out"], full["out"][sub], rtol=1e-13, atol=1e-14)
+    np.testing.assert_array_equal(part["pos"], full["pos"])
+
+
+# ---------------------------------------------------------------- Lab invariants
+
+def test_lab1_invariants_no_drop():
+    """Lab 1: every token reaches exactly k experts; more than one expert is used."""
+    L = _tiny_layer(8, T=20, d=6, E=8)
+    res = O.forward(L["x"], L["W_g"], 2, O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"], C=20)
+    assert int(res["counts"].sum()) == 20 * 2 and res["dropped"] == 0
+    assert (res["counts"] > 0).sum() >= 2
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_lab3_capacity_behaviour(seed):
+    """Lab 3: balanced routing with factor 1.5 drops < 5%; skewed routing with
+    factor 1.0 drops more; no expert exceeds its capacity."""
+    rng = np.random.default_rng(100 + seed)
+    n, E = 100, 4
+    balanced = rng.integers(0, E, size=n)
+    skewed = np.concatenate([np.zeros(60, dtype=np.int64), rng.integers(1, E, size=40)])
+    rng.shuffle(skewed)
+    Ca = O.capacity(n, 1, E, 1.5)
+    Cb = O.capacity(n, 1, E, 1.0)
+    da = O.dispatch(balanced[:, None], E, Ca)
+    db = O.dispatch(skewed[:, None], E, Cb)
+    ra, rb = da["dropped"] / n, db["dropped"] / n
+    assert ra < 0.05 and rb > ra
+    assert da["counts"].max() <= Ca and db["counts"].max() <= Cb
+
+
+def test_near_tie_report():
+    H = np.array([[1.0, 1.00005, 0.0, -1.0],   # adjacent inside top-2
+                  [2.0, 1.0, 0.99995, -1.0],   # boundary k-th vs (k+1)-th
+                  [3.0, 2.0, 1.0, 0.0]])
+    r = O.near_ties(H, 2)
+    assert r["boundary"].tolist() == [1]
+    assert r["any_adjacent"].tolist() == [0, 1]
+
+
+def test_workload_generator_is_deterministic():
+    w = W.WORKLOADS["tiny_fp32"]
+    a, b = W.make_inputs(w), W.make_inputs(w)
+    for key in a:
+        if a[key] is None:
+            assert b[key] is None
+        else:
+            assert torch.equal(a[key], b[key])
+    s = W.make_inputs(W.WORKLOADS["switch_top1"].scaled(64))
+    np.testing.assert_allclose(s["b_g"].numpy()[:3], [0.0, 2 * math.log(0.5), 2 * math.log(1 / 3)], rtol=1e-6)
