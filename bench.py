@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Throughput of the sparse MoE layer forward pass on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one whole layer forward (router, top-k, capacity dispatch + gather,
+expert GEMMs, combine) over one batch of seeded synthetic tokens already
+resident in HBM.  L2 is flushed (256 MiB write) between timed steps, outside
+the measured events.  Prints one JSON line.
+
+--impl reference times the fp64 CPU oracle instead (the reference arm of this
+benchmark), on the host cores, each step a bounded sub-batch of the workload.
+For N > 1 (torchrun) every rank runs an independent replica of the layer on
+its own GPU and batch: the path has no exchange step, so there is no
+collective on the data path; ranks only meet at the barriers around the
+timed region and in the max-over-ranks of the elapsed time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer fwd tokens/s on 1 B300; TFLOP/s or HBM GB/s as % of roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "bf16_t4096"
+KERNELS_PER_STEP = 6  # router, dispatch, gather, expert GEMM 1, expert GEMM 2, combine
+FLUSH_BYTES = 256 << 20
+
+# DRAM traffic of the dominant kernel per launch, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
+# hash of the kernel sources it was taken on; a changed kernel reports null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+GEMM_SOURCES = ["sparse_mixture_experts_51_b300/csrc/gemm_tc.cu", "sparse_mixture_experts_51_b300/csrc/common.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def gemm1_work(w, counts):
+    """Algorithmic flops and DRAM bytes of the first expert GEMM (dominant kernel)
+    for the kept rows: flops 2*d*F per row (x2 for SwiGLU's gate and up),
+    bytes = weights of every expert with a kept row + grouped rows read + hidden written."""
+    from sparse_mixture_experts_51_b300 import workloads as W
+    R = int(sum(counts))
+    active = sum(1 for c in counts if c > 0)
+    b = 2 if w.dtype_name == "bf16" else 4
+    mats = 2 if w.act == W.ACT_SWIGLU else 1
+    flops = float(R) * 2.0 * w.d * w.F * mats
+    nbytes = float(active) * mats * w.F * w.d * b + float(R) * w.d * b + float(R) * w.F * b
+    return flops, nbytes
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+    def __init__(self, index: int, period_s: float = 0.01):
+        self.samples = []
+        self.max_mhz = None
+        self.ok = False
+        self._stop = threading.Event()
+        self.period = period_s
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # NVML missing: report it rather than guess
+            self.err = repr(e)
+
+    def _reasons(self):
+        nv = self.nv
+        fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return fn(self.h)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                util = self.nv.nvmlDeviceGetUtilizationRates(self.h).gpu
+                self.samples.append((mhz, int(self._reasons()), util))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+        busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
+        mhz = [s[0] for s in busy]
+        bits = 0
+        for s in busy:
+            bits |= s[1]
+        reasons = [name for bit, name in self.REASONS.items() if bits & bit and bit != 0x1]
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(busy)}
+
+
+_ORACLE_CACHE = {}
+
+
+def cpu_oracle_run(w, budget_s: float):
+    """Time the fp64 oracle, as it stands, on a sub-batch of the workload (the
+    same layer with its first T_s tokens as their own batch) for about
+    budget_s seconds.  Returns (tokens/s, sample description, threads, seconds)."""
+    from oracle import moe_oracle as O
+    from sparse_mixture_experts_51_b300 import workloads as W
+
+    class F64:
+        def __init__(self, t):
+            self.t = t
+            self.cache = {}
+
+        def __getitem__(self, e):
+            if e not in self.cache:
+                self.cache[e] = W.as_f64_numpy(self.t[e])
+            return self.cache[e]
+
+    # sub-batch size from the algorithmic work per token (fp64 BLAS ~1e11 flop/s)
+    per_tok = 2.0 * w.d * w.F * (3 if w.act == W.ACT_SWIGLU else 2) * w.k + 2.0 * w.d * w.E
+    T_s = int(max(16, min(w.T, budget_s * 1e11 / per_tok / 2)))
+    key = (w.name, T_s)
+    if key not in _ORACLE_CACHE:
+        inp = W.make_inputs(w.scaled(T_s))
+        f = W.as_f64_numpy
+        _ORACLE_CACHE[key] = (f(inp["x"]), f(inp["W_g"]), F64(inp["W1"]), F64(inp["W2"]), dict(
+            W3=None if inp["W3"] is None else F64(inp["W3"]), b1=None if inp["b1"] is None else F64(inp["b1"]),
+            b2=None if inp["b2"] is None else F64(inp["b2"]), b_g=f(inp["b_g"]), W_noise=f(inp["W_noise"]),
+            eps=f(inp["eps"]), capacity_factor=w.capacity_factor))
+    x, Wg, W1, W2, args = _ORACLE_CACHE[key]
+    runs, tokens, t0 = 0, 0, time.perf_counter()
+    while True:
+        O.forward(x, Wg, w.k, w.act, W1, W2, **args)
+        runs += 1
+        tokens += T_s
+        el = time.perf_counter() - t0
+        if el >= budget_s or runs >= 1000:
+            break
+    cores = os.cpu_count()
+    sample = (f"{runs} oracle forward(s) of a {T_s}-token sub-batch of {w.name} (its own capacity "
+              f"ceil({w.capacity_factor}*{T_s}*{w.k}/{w.E})), fp64 NumPy, BLAS on all host threads")
+    return tokens / el, sample, cores, el
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(a):
+    """Reference arm: the fp64 CPU oracle, timed on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from sparse_mixture_experts_51_b300 import workloads as W
+    w = W.WORKLOADS[a.workload]
+    per_step = max(0.5, min(10.0, 150.0 / max(1, a.steps + a.warmup)))
+    for i in range(a.warmup):
+        cpu_oracle_run(w, per_step * 0.2)
+    vals, total_t, total_tok = [], 0.0, 0.0
+    sample = ""
+    cores = os.cpu_count()
+    for i in range(a.steps):
+        v, sample, cores, el = cpu_oracle_run(w, per_step)
+        vals.append(v)
+        total_t += el
+        total_tok += v * el
+    value = total_tok / total_t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": a.gpus, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": 1e3 * total_t / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(w):
+    from sparse_mixture_experts_51_b300 import workloads as W
+    return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
+            "act": "swiglu" if w.act == W.ACT_SWIGLU else "gelu", "capacity_factor": w.capacity_factor,
+            "noisy_gating": w.noisy, "dtype": w.dtype_name, "seed": w.seed,
+            "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
+
+
+def run_ours(a):
+    import ctypes
+
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mixture_experts_51_b300 import _lib, api
+    from sparse_mixture_experts_51_b300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    lib = _lib.load()
+
+    w = W.WORKLOADS[a.workload]
+    if world > 1:
+        w = w.with_(seed=w.seed + 1000 * rank)  # an independent replica batch per rank
+    inp = W.make_inputs(w)
+    g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
+    C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
+    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act)
+    ws = api.new_workspace(shape, C, dev)
+    out = torch.empty(w.T, w.d, dtype=w.dtype, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    dropped = torch.empty(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    P = api._ptr
+
+    def fwd_args():
+        return [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
+                P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), P(out),
+                None, None, None, None, P(counts), None, P(dropped), None, P(ws), ws.numel(), sptr]
+
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
+
+    def step_timed(i):
+        arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in stage_ev[i]])
+        _lib.check(lib.moe_forward_timed(*fwd_args(), arr), "moe_forward_timed")
+
+    # make sure every event exists on the device before its handle is used
+    for evs in stage_ev:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    for _ in range(a.warmup):
+        _lib.check(lib.moe_forward(*fwd_args()), "moe_forward")
+        flush.zero_()
+    torch.cuda.synchronize()
+    assert api.get_device_error(ws) == 0
+
+    sampler = ClockSampler(local)
+    with sampler:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(a.steps):
+            flush.zero_()
+            step_timed(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+    err = api.get_device_error(ws)
+    if err != 0:
+        raise RuntimeError(f"device-side error {err} during the timed region")
+
+    step_ms = [evs[0].elapsed_time(evs[5]) for evs in stage_ev]
+    stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev] for j in range(5)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_all = w.T * a.steps * world
+    value = tokens_all / (total_ms / 1e3)
+
+    # ---------------- roofline of the dominant kernel (first expert GEMM)
+    cnt = counts.cpu().tolist()
+    flops, nbytes = gemm1_work(w, cnt)
+    g1_ms = statistics.mean(stage_ms[2])
+    peaks = load_peaks()
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as fh:
+            rec = json.load(fh).get(w.name)
+        if rec and rec.get("kernel_hash") == kernel_hash():
+            traffic = rec.get("dram_bytes_per_launch")
+    if flops / nbytes >= ridge:
+        achieved = flops / (g1_ms / 1e3) / 1e12
+        roof = {"kernel": "grouped_gemm_kernel (expert GEMM 1, fused activation)", "bound": "tensor",
+                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "peak_source": peaks["source"] + " bf16 burst",
+                "algorithmic_flops": flops, "ms_per_launch": g1_ms, "traffic": traffic}
+    else:
+        achieved = nbytes / (g1_ms / 1e3) / 1e9
+        roof = {"kernel": "grouped_gemm_kernel (expert GEMM 1, fused activation)", "bound": "hbm",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy bandwidth",
+                "algorithmic_bytes": nbytes, "ms_per_launch": g1_ms, "traffic": traffic}
+
+    # ---------------- end to end through the public API with host buffers
+    layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
+                         b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False)
+    x_host = inp["x"].pin_memory()
+    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
+    out_host = torch.empty(w.T, w.d, dtype=w.dtype).pin_memory()
+    x_dev = torch.empty_like(g["x"])
+    eps_dev = torch.empty_like(g["eps"]) if g["eps"] is not None else None
+    out_dev = torch.empty_like(out)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        if eps_dev is not None:
+            eps_dev.copy_(eps_host, non_blocking=True)
+        layer(x_dev, eps=eps_dev, out=out_dev)
+        out_host.copy_(out_dev, non_blocking=True)
+
+    for _ in range(max(1, a.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = 0.0
+    n_e2e = max(1, a.steps)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+    for i in range(n_e2e):
+        flush.zero_()
+        evs[i][0].record(stream)
+        e2e_step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in evs)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e = {"value": w.T * n_e2e * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+
+    cpu = None
+    if not a.no_cpu_baseline and world == 1:
+        v, sample, cores, _ = cpu_oracle_run(w, a.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    cfg = workload_config(w)
+    cfg.update({"C": C, "kept_rows": int(sum(cnt)), "dropped": int(dropped.item()),
+                "parallelism": "replicas" if world > 1 else "single_gpu"})
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+            "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype_name, "data": "synthetic", "config": cfg,
+            "stage_ms": {n: statistics.mean(v) for n, v in zip(
+                ["router", "dispatch_gather", "expert_gemm1", "expert_gemm2", "combine"], stage_ms)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * a.steps,
+            "clocks": sampler.summary()}
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    a = parse_args(argv)
+    if a.impl == "reference":
+        return run_reference(a)
+    return run_ours(a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,223 @@
+/*
+ * moe_b300.h -- C ABI of the B300 (sm_103a) sparse Mixture-of-Experts layer
+ * forward pass.
+ *
+ * The layer, step by step (pages cited by title and section):
+ *   1. router logits      H = x W_g + b_g + eps * softplus(x W_noise)
+ *                         ("LLM part 09: Sparse Mixture-of-Experts (MoE)",
+ *                         s2 noisy top-k gating; "Mixture-of-Experts Sparse
+ *                         Model Scaling", Mathematical Formulation)
+ *   2. top-k + gates      idx = k largest H (ties -> lower expert index),
+ *                         w = softmax over the k selected logits
+ *                         (same s2; "Mixture-of-experts Models", Level 2
+ *                         "Router scores become a sparse dispatch decision")
+ *   3. dispatch           capacity C = ceil(cf*T*k/E) ("3D mixture-of-experts
+ *                         routing lab", Capacity card); first-come slots in
+ *                         rank-major priority order (every token's first
+ *                         choice before any second choice, tokens in order);
+ *                         over-capacity assignments dropped
+ *                         ("Mixture-of-Experts Sparse Model Scaling", Lab 3
+ *                         and Advanced Theory; "Mixture-of-experts Models",
+ *                         "Capacity limits make dispatch observable")
+ *   4. experts            GELU:   y = gelu(x W1^T + b1) W2^T + b2
+ *                         SwiGLU: y = (silu(x W1^T) * (x W3^T)) W2^T + b2
+ *   5. combine            out[t] = residual[t] + sum_{kept r} w[t,r] y_{t,r}
+ *                         ("LLM part 09", s1 y = sum_i G(x)_i E_i(x); s3:
+ *                         a dropped assignment bypasses its expert and the
+ *                         residual carries the token)
+ *
+ * Conventions for every entry point
+ *   - All tensor arguments are DEVICE pointers of the current CUDA device,
+ *     row-major, densely packed, owned by the caller.  The library never
+ *     allocates, frees, or synchronises (except moe_get_device_error) and
+ *     keeps no per-call state outside the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy stream).
+ *     All work is enqueued on it; every call returns before the GPU is done.
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned as MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *     MOE_ERR_WORKSPACE.  A CUDA runtime failure returns MOE_ERR_CUDA.
+ *     Errors found on the device (a bounded wait that gave up, an index out
+ *     of range) are recorded in the workspace's error word and read back
+ *     with moe_get_device_error(); kernels never trap or abort.
+ *   - dtype MOE_F32: x, expert weights, out are fp32 (CUDA-core path,
+ *     intended for small layers).  MOE_BF16: x, W1, W3, W2, out are bf16,
+ *     expert GEMMs run on the tcgen05 tensor cores with fp32 accumulation;
+ *     needs d and d_ff multiples of 64.  Router tensors (W_g, b_g, W_noise,
+ *     eps), gates, expert biases and the per-assignment expert outputs are
+ *     fp32 for both dtypes.
+ *   - Limits: 1 <= E <= 128, 1 <= k <= min(E, 16), 1 <= d, d_ff,
+ *     0 <= T < 2^31 / k.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null pointer, bad size, k > E, ...          */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid but outside the supported set         */
+  MOE_ERR_WORKSPACE = 3,      /* workspace null, misaligned or too small     */
+  MOE_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed           */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait gave up          */
+  MOE_ERR_BOUNDS = 6          /* a device-side index check failed            */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
+
+/* Shape of one layer call.  T tokens of width d, E experts of hidden width
+ * d_ff, top-k routing.  dtype is a moe_dtype_t, act a moe_act_t. */
+typedef struct {
+  int64_t T;
+  int32_t d;
+  int32_t E;
+  int32_t k;
+  int32_t d_ff;
+  int32_t dtype;
+  int32_t act;
+} moe_shape_t;
+
+/* Expert capacity C = ceil(capacity_factor * T * k / E), evaluated in double
+ * in that order ("3D mixture-of-experts routing lab", Capacity card; the
+ * k = 1 form is "LLM part 09", s3).  Returns -1 for T < 0, k < 1, E < 1 or a
+ * capacity factor that is not finite and positive, or a result that does
+ * not fit in int32. */
+MOE_API int32_t moe_capacity(int64_t T, int32_t k, int32_t E, double capacity_factor);
+
+/* Rows of the expert-grouped buffers for capacity C: min(T*k, E*C). */
+MOE_API int64_t moe_max_rows(const moe_shape_t* shape, int32_t C);
+
+/* Workspace bytes that moe_forward needs for this shape and capacity (it
+ * also covers moe_dispatch and moe_expert_ffn).  The workspace is a device
+ * buffer of at least this many bytes, 256-byte aligned, ZERO-FILLED ONCE
+ * after allocation; the library keeps its control words consistent after
+ * that.  Returns MOE_ERR_INVALID_ARG for a bad shape or C < 0. */
+MOE_API moe_status_t moe_workspace_size(const moe_shape_t* shape, int32_t C, size_t* bytes);
+
+/* Step 1+2: router logits, top-k and gates, for every token.
+ *   x        [T,d]  dtype        tokens
+ *   W_g      [d,E]  fp32         router weight
+ *   b_g      [E]    fp32 | NULL  router bias (NULL = none)
+ *   W_noise  [d,E]  fp32 | NULL  noise projection; with eps, adds
+ *   eps      [T,E]  fp32 | NULL  eps * softplus(x W_noise) to the logits
+ *   idx      [T,k]  int32 out    selected experts, largest logit first
+ *   w        [T,k]  fp32  out    gates (softmax over the selected logits)
+ *   logits   [T,E]  fp32 | NULL  out: the (noisy) logits, computed in fp32
+ *   stats    [2]    int64 | NULL out, ADDED to: [0] tokens whose selection
+ *                   was settled by the fp64 re-evaluation, [1] tokens whose
+ *                   k-th and (k+1)-th fp32 logits differ by < 1e-4
+ * Selection is exact: logits are computed in fp32 together with a rigorous
+ * error bound; a token whose order is not settled by the bound has its
+ * candidate logits re-evaluated in fp64, so idx equals the top-k of the
+ * exactly computed logits (up to fp64 rounding).  W_noise and eps must be
+ * both NULL or both set. */
+MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g,
+                       const float* b_g, const float* W_noise, const float* eps,
+                       int32_t* idx, float* w, float* logits, int64_t* stats,
+                       void* stream);
+
+/* Step 3: capacity-limited dispatch and the gather into expert order.
+ *   C         capacity (moe_capacity, or any C >= 0)
+ *   idx       [T,k]  int32        from moe_route (values in [0,E))
+ *   x         [T,d]  dtype        tokens
+ *   pos       [T,k]  int32 out    slot of (t,r) inside expert idx[t,r]'s
+ *                                 segment, -1 if the assignment was dropped
+ *   counts    [E]    int32 out    kept assignments per expert, min(load, C)
+ *   offsets   [E+1]  int32 out    exclusive prefix sum of counts
+ *   dropped   [1]    int64 out    sum_e max(0, load_e - C)
+ *   x_perm    [moe_max_rows,d] dtype out   row offsets[e]+pos[t,r] = x[t]
+ *   row_token [moe_max_rows] int32 | NULL  out: token of each row
+ *   ws, ws_bytes  workspace (moe_workspace_size)
+ * Results are deterministic (no atomics decide any slot).  An expert id
+ * outside [0,E) sets MOE_ERR_BOUNDS in the error word; that assignment gets
+ * pos = -1 and is counted in no load. */
+MOE_API moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int32_t* idx,
+                          const void* x, int32_t* pos, int32_t* counts, int32_t* offsets,
+                          int64_t* dropped, void* x_perm, int32_t* row_token,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4: every expert's FFN over its segment of the expert-grouped rows.
+ *   x_perm   [moe_max_rows,d]  dtype   grouped rows (moe_dispatch)
+ *   offsets  [E+1] int32               segment starts (moe_dispatch)
+ *   W1       [E,d_ff,d] dtype          up projection (GELU) / gate (SwiGLU)
+ *   W3       [E,d_ff,d] dtype | NULL   SwiGLU up projection (NULL for GELU)
+ *   W2       [E,d,d_ff] dtype          down projection
+ *   b1       [E,d_ff] fp32 | NULL      GELU only (must be NULL for SwiGLU)
+ *   b2       [E,d]    fp32 | NULL
+ *   y_perm   [moe_max_rows,d] fp32 out expert output of each grouped row;
+ *                                      rows past offsets[E] are untouched
+ *   ws, ws_bytes  workspace (holds the [moe_max_rows,d_ff] hidden activations)
+ * bf16: the hidden activation is rounded to bf16 between the two GEMMs. */
+MOE_API moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const void* x_perm,
+                            const int32_t* offsets, const void* W1, const void* W3,
+                            const void* W2, const float* b1, const float* b2,
+                            float* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 5: weighted combine into the residual, one token at a time, ranks
+ * summed in order 0..k-1 (deterministic).
+ *   y_perm   [moe_max_rows,d] fp32   expert outputs (moe_expert_ffn)
+ *   idx, w, pos [T,k], offsets [E+1]  as produced above
+ *   residual [T,d] dtype | NULL       NULL = zero residual
+ *   out      [T,d] dtype out          residual + moe
+ *   moe_out  [T,d] fp32 | NULL out    the weighted expert sum alone */
+MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_perm,
+                         const int32_t* idx, const float* w, const int32_t* pos,
+                         const int32_t* offsets, const void* residual, void* out,
+                         float* moe_out, void* stream);
+
+/* The whole layer: steps 1-5 on one stream, residual = x.
+ *   capacity_factor  used when C_override < 0; else C = C_override
+ *   x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2   as above
+ *   out [T,d] dtype out; moe_out [T,d] fp32 | NULL out
+ *   idx, w, pos [T,k], counts [E], offsets [E+1], dropped [1], stats [2]:
+ *     optional outputs (NULL = keep them in the workspace only; stats as
+ *     in moe_route, added to)
+ *   ws, ws_bytes  workspace of moe_workspace_size(shape, C) bytes */
+MOE_API moe_status_t moe_forward(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
+                         const void* x, const float* W_g, const float* b_g,
+                         const float* W_noise, const float* eps, const void* W1,
+                         const void* W3, const void* W2, const float* b1, const float* b2,
+                         void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
+                         int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* moe_forward, recording six CUDA events (cudaEvent_t, created by the
+ * caller) on `stream` at the stage boundaries, so each stage can be timed
+ * with cudaEventElapsedTime:
+ *   stage_events[0] before the router        [1] after the router
+ *   [2] after dispatch + gather              [3] after the first expert GEMM
+ *   [4] after the second expert GEMM         [5] after the combine
+ * MOE_ERR_INVALID_ARG if stage_events or any of its six entries is NULL. */
+MOE_API moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
+                                       const void* x, const float* W_g, const float* b_g,
+                                       const float* W_noise, const float* eps, const void* W1,
+                                       const void* W3, const void* W2, const float* b1, const float* b2,
+                                       void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
+                                       int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
+                                       void* ws, size_t ws_bytes, void* stream, void* const* stage_events);
+
+/* Synchronises `stream`, reads the workspace's device error word, clears it,
+ * and returns it as a status (MOE_OK when no device-side error was recorded
+ * since the last read).  `ws` is the workspace passed to the calls. */
+MOE_API moe_status_t moe_get_device_error(void* ws, void* stream);
+
+/* Static, human-readable name of a status code. */
+MOE_API const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

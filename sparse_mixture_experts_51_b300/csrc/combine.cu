@@ -1,0 +1,174 @@
+// Weighted combine into the residual, and the fp32 CUDA-core expert FFN.
+//
+// Combine: out[t] = residual[t] + sum over kept ranks r (in order 0..k-1) of
+// w[t,r] * y_perm[offsets[idx[t,r]] + pos[t,r]]  ("LLM part 09: Sparse
+// Mixture-of-Experts (MoE)", s1 output equation and s3 residual bypass of
+// dropped tokens; "Mixture-of-Experts Sparse Model Scaling", Lab 1 weighted
+// accumulation).  One warp per token gathers its k expert rows with 16-byte
+// loads and writes the token once: deterministic, no atomics.
+//
+// fp32 FFN: the grouped expert MLP on CUDA cores for fp32 layers (whose
+// tolerance rules out tf32/bf16 tensor cores): one warp per output element,
+// lanes split the reduction so every weight row is read with coalesced loads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+template <typename TO>
+__device__ __forceinline__ void load4(const TO* p, float (&v)[4]);
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+  const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <typename TO>
+__device__ __forceinline__ void store4(TO* p, const float (&v)[4]);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4]) {
+  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
+  *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(h);
+}
+
+template <typename TO>
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+  const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (t >= p.T) return;
+  const int k = p.k, d = p.d;
+  long long row[kMaxTopK];
+  float wt[kMaxTopK];
+#pragma unroll
+  for (int r = 0; r < kMaxTopK; ++r) {
+    row[r] = -1;
+    wt[r] = 0.f;
+    if (r < k) {
+      const int ps = p.pos[t * k + r];
+      if (ps >= 0) {
+        const int e = p.idx[t * k + r];
+        long long rw = -1;
+        if (e >= 0 && e < p.E) rw = static_cast<long long>(p.offsets[e]) + ps;
+        if (rw < 0 || rw >= p.rows) {
+          if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
+          rw = -1;
+        }
+        row[r] = rw;
+        wt[r] = p.w[t * k + r];
+      }
+    }
+  }
+  const TO* res = static_cast<const TO*>(p.residual);
+  TO* out = static_cast<TO*>(p.out);
+  for (int c = lane * 4; c < d; c += 128) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kMaxTopK; ++r) {
+      if (r < k && row[r] >= 0) {
+        float y[4];
+        const float4 q = __ldg(reinterpret_cast<const float4*>(p.y_perm + row[r] * d + c));
+        y[0] = q.x; y[1] = q.y; y[2] = q.z; y[3] = q.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wt[r], y[i], acc[i]);
+      }
+    }
+    if (p.moe_out) store4<float>(p.moe_out + t * d + c, acc);
+    float o[4] = {acc[0], acc[1], acc[2], acc[3]};
+    if (res) {
+      float rv[4];
+      load4<TO>(res + t * d + c, rv);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) o[i] = rv[i] + acc[i];
+    }
+    store4<TO>(out + t * d + c, o);
+  }
+}
+
+// index of the expert whose segment [offsets[e], offsets[e+1]) holds `row`
+__device__ __forceinline__ int expert_of_row(const int32_t* offsets, int E, long long row) {
+  int lo = 0, hi = E;  // offsets[lo] <= row < offsets[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (offsets[mid] <= row) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// h[row, f] = act(x_perm[row] . W1[e, f] (+ b1[e, f]))   (SwiGLU: silu(.) * x_perm[row] . W3[e, f])
+__global__ void __launch_bounds__(256) ffn1_f32_kernel(FfnParams p) {
+  const long long row = blockIdx.x;
+  const int f = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int32_t* off = p.offsets;
+  if (row >= off[p.E] || f >= p.F) return;
+  const int e = expert_of_row(off, p.E, row);
+  const float* xr = static_cast<const float*>(p.x_perm) + row * p.d;
+  const float* w1 = static_cast<const float*>(p.W1) + (static_cast<long long>(e) * p.F + f) * p.d;
+  float a = 0.f, u = 0.f;
+  for (int j = lane; j < p.d; j += 32) a = fmaf(xr[j], w1[j], a);
+  a = warp_sum(a);
+  float h;
+  if (p.act == MOE_ACT_SWIGLU) {
+    const float* w3 = static_cast<const float*>(p.W3) + (static_cast<long long>(e) * p.F + f) * p.d;
+    for (int j = lane; j < p.d; j += 32) u = fmaf(xr[j], w3[j], u);
+    u = warp_sum(u);
+    h = a / (1.0f + expf(-a)) * u;
+  } else {
+    if (p.b1) a += p.b1[static_cast<long long>(e) * p.F + f];
+    h = 0.5f * a * (1.0f + erff(a * 0.70710678118654752f));
+  }
+  if (lane == 0) static_cast<float*>(p.h)[row * p.F + f] = h;
+}
+
+// y_perm[row, i] = h[row] . W2[e, i] (+ b2[e, i])
+__global__ void __launch_bounds__(256) ffn2_f32_kernel(FfnParams p) {
+  const long long row = blockIdx.x;
+  const int i = blockIdx.y * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int32_t* off = p.offsets;
+  if (row >= off[p.E] || i >= p.d) return;
+  const int e = expert_of_row(off, p.E, row);
+  const float* hr = static_cast<const float*>(p.h) + row * p.F;
+  const float* w2 = static_cast<const float*>(p.W2) + (static_cast<long long>(e) * p.d + i) * p.F;
+  float a = 0.f;
+  for (int j = lane; j < p.F; j += 32) a = fmaf(hr[j], w2[j], a);
+  a = warp_sum(a);
+  if (p.b2) a += p.b2[static_cast<long long>(e) * p.d + i];
+  if (lane == 0) p.y_perm[row * p.d + i] = a;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t st) {
+  if (p.T == 0) return cudaSuccess;
+  const long long blocks = (static_cast<long long>(p.T) * 32 + 255) / 256;
+  if (p.dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  else
+    combine_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st) {
+  if (p.rows == 0) return cudaSuccess;
+  dim3 g1(static_cast<unsigned>(p.rows), static_cast<unsigned>((p.F + 7) / 8));
+  ffn1_f32_kernel<<<g1, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2(static_cast<unsigned>(p.rows), static_cast<unsigned>((p.d + 7) / 8));
+  ffn2_f32_kernel<<<g2, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,283 @@
+// Capacity-limited dispatch and the gather into expert order.
+//
+// Semantics ("Mixture-of-Experts Sparse Model Scaling", Lab 3 and Advanced
+// Theory; "Mixture-of-experts Models", "Capacity limits make dispatch
+// observable"): assignments are taken in priority order j = r*T + t (every
+// token's first choice, in token order, before any second choice); an
+// assignment gets the next slot of its expert while fewer than C slots are
+// taken, and is dropped otherwise.  pos[t,r] = number of earlier assignments
+// to the same expert, kept iff pos < C.
+//
+// Design.  One pass, deterministic, no atomics deciding any slot:
+//   * each block takes a tile of 4096 consecutive priority positions; a block
+//     obtains its tile index from a ticket counter, so a block only ever
+//     waits on blocks that are already running;
+//   * inside the tile, 16 steps of 256 assignments: warps rank equal experts
+//     with match.any + popc, a per-warp histogram in shared memory orders the
+//     warps, and a running per-expert count orders the steps;
+//   * the per-expert block totals are scanned across blocks with a
+//     decoupled look-back over E-wide descriptors (aggregate / inclusive
+//     prefix); every wait is bounded and records MOE_ERR_DEVICE_TIMEOUT;
+//   * the block holding the last tile turns the loads into counts, segment
+//     offsets and the drop count.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int NT = kDispatchThreads;
+constexpr int ITEMS = kDispatchItemsPerThread;
+constexpr int NWARP = NT / 32;
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
+  __shared__ int s_cnt[kMaxExperts];            // running count per expert in this tile
+  __shared__ int s_whist[NWARP][kMaxExperts];   // this step's count per warp and expert
+  __shared__ int s_excl[kMaxExperts];           // assignments to each expert before this tile
+  __shared__ int s_ticket;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E;
+  const long long total = static_cast<long long>(p.T) * p.k;
+
+  if (tid == 0) s_ticket = atomicAdd(&p.ctrl[0], 1);
+  for (int i = tid; i < kMaxExperts; i += NT) s_cnt[i] = 0;
+  for (int i = tid; i < NWARP * kMaxExperts; i += NT) (&s_whist[0][0])[i] = 0;
+  __syncthreads();
+  const int b = s_ticket;
+  int* status = p.ctrl + 1;
+  const long long base = static_cast<long long>(b) * (NT * ITEMS);
+
+  int my_e[ITEMS], my_rank[ITEMS];
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const long long j = base + static_cast<long long>(i) * NT + tid;
+    int e = -1;
+    if (j < total) {
+      const int r = static_cast<int>(j / p.T);
+      const int t = static_cast<int>(j - static_cast<long long>(r) * p.T);
+      e = p.idx[static_cast<long long>(t) * p.k + r];
+      if (e < 0 || e >= E) {
+        record_error(p.err, MOE_ERR_BOUNDS);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_in_warp = __popc(peers & lt_mask);
+    if (e >= 0 && rank_in_warp == 0) s_whist[warp][e] = __popc(peers);
+    __syncthreads();
+    int rank = 0;
+    if (e >= 0) {
+      rank = s_cnt[e] + rank_in_warp;
+      for (int w2 = 0; w2 < warp; ++w2) rank += s_whist[w2][e];
+    }
+    my_e[i] = e;
+    my_rank[i] = rank;
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += NT) {
+      int sum = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < NWARP; ++w2) {
+        sum += s_whist[w2][ex];
+        s_whist[w2][ex] = 0;
+      }
+      s_cnt[ex] += sum;
+    }
+    __syncthreads();
+  }
+
+  // ---- publish this tile's per-expert totals, then look back for the prefix
+  int* agg = p.agg + static_cast<long long>(b) * E;
+  int* incl = p.incl + static_cast<long long>(b) * E;
+  for (int ex = tid; ex < E; ex += NT) {
+    __stcg(&agg[ex], s_cnt[ex]);
+    if (b == 0) __stcg(&incl[ex], s_cnt[ex]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0 && b != p.stall_block) st_release(&status[b], b == 0 ? 2 : 1);
+
+  if (warp == 0) {
+    constexpr int SL = kMaxExperts / 32;
+    int ex_acc[SL];
+#pragma unroll
+    for (int s = 0; s < SL; ++s) ex_acc[s] = 0;
+    int pred = b - 1;
+    bool timed_out = false;
+    while (pred >= 0) {
+      int f = 0;
+      if (lane == 0) {
+        const unsigned long long t0 = globaltimer_ns();
+        unsigned spins = 0;
+        while ((f = ld_acquire(&status[pred])) == 0) {
+          if ((++spins & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+      }
+      f = __shfl_sync(0xffffffffu, f, 0);
+      if (f == 0) {
+        timed_out = true;
+        break;
+      }
+      __threadfence();
+      const int* src = (f == 2 ? p.incl : p.agg) + static_cast<long long>(pred) * E;
+#pragma unroll
+      for (int s = 0; s < SL; ++s) {
+        const int ex = lane + 32 * s;
+        if (ex < E) ex_acc[s] += __ldcg(&src[ex]);
+      }
+      if (f == 2) break;
+      --pred;
+    }
+    if (timed_out && lane == 0) record_error(p.err, MOE_ERR_DEVICE_TIMEOUT);
+#pragma unroll
+    for (int s = 0; s < SL; ++s) {
+      const int ex = lane + 32 * s;
+      if (ex < E) {
+        s_excl[ex] = ex_acc[s];
+        if (b > 0) __stcg(&incl[ex], ex_acc[s] + s_cnt[ex]);
+      }
+    }
+    __threadfence();
+    __syncwarp();
+    if (b > 0 && lane == 0 && b != p.stall_block) st_release(&status[b], 2);
+  }
+  __syncthreads();
+
+  // ---- slots: earlier tiles + rank inside this tile; kept iff below capacity
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const long long j = base + static_cast<long long>(i) * NT + tid;
+    if (j < total) {
+      const int r = static_cast<int>(j / p.T);
+      const int t = static_cast<int>(j - static_cast<long long>(r) * p.T);
+      int ps = -1;
+      if (my_e[i] >= 0) {
+        const int slot = s_excl[my_e[i]] + my_rank[i];
+        ps = slot < p.C ? slot : -1;
+      }
+      p.pos[static_cast<long long>(t) * p.k + r] = ps;
+    }
+  }
+
+  // ---- the last tile knows every expert's load
+  if (b == p.nblk - 1) {
+    __shared__ int s_counts[kMaxExperts];
+    __shared__ unsigned long long s_drop[NWARP];
+    unsigned long long drop = 0;
+    for (int ex = tid; ex < kMaxExperts; ex += NT) {
+      int c = 0;
+      if (ex < E) {
+        const int load = s_excl[ex] + s_cnt[ex];
+        c = load < p.C ? load : p.C;
+        drop += static_cast<unsigned long long>(load - c);
+        p.counts[ex] = c;
+      }
+      s_counts[ex] = c;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) drop += __shfl_xor_sync(0xffffffffu, drop, o);
+    if (lane == 0) s_drop[warp] = drop;
+    __syncthreads();
+    if (warp == 0) {
+      // exclusive scan of counts over E <= 128 experts, 4 per lane
+      int v[4], run = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        v[q] = s_counts[lane * 4 + q];
+        run += v[q];
+      }
+      int incl_sum = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl_sum, o);
+        if (lane >= o) incl_sum += n;
+      }
+      int off = incl_sum - run;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ex = lane * 4 + q;
+        if (ex < E) p.offsets[ex] = off;
+        off += v[q];
+      }
+      if (lane == 31) p.offsets[E] = incl_sum;
+      if (lane == 0) {
+        unsigned long long dsum = 0;
+        for (int w2 = 0; w2 < NWARP; ++w2) dsum += s_drop[w2];
+        *p.dropped = static_cast<long long>(dsum);
+      }
+    }
+  }
+}
+
+// One warp per assignment (t, r): copy token t into its expert-ordered row.
+template <int VB>
+__global__ void __launch_bounds__(256) gather_kernel(GatherParams p, long long rows_alloc) {
+  const long long a = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long total = static_cast<long long>(p.T) * p.k;
+  if (a >= total) return;
+  const int ps = p.pos[a];
+  if (ps < 0) return;
+  const int e = p.idx[a];
+  if (e < 0 || e >= p.E) {
+    if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
+    return;
+  }
+  const long long row = static_cast<long long>(p.offsets[e]) + ps;
+  if (row < 0 || row >= rows_alloc) {
+    if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
+    return;
+  }
+  const long long t = a / p.k;
+  const long long row_bytes = static_cast<long long>(p.d) * p.elem_bytes;
+  const char* src = static_cast<const char*>(p.x) + t * row_bytes;
+  char* dst = static_cast<char*>(p.x_perm) + row * row_bytes;
+  if constexpr (VB == 16) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    const long long n = row_bytes / 16;
+    for (long long i = lane; i < n; i += 32) d4[i] = __ldg(&s4[i]);
+  } else {
+    const long long n = row_bytes / 4;
+    const uint32_t* s1 = reinterpret_cast<const uint32_t*>(src);
+    uint32_t* d1 = reinterpret_cast<uint32_t*>(dst);
+    for (long long i = lane; i < n; i += 32) d1[i] = __ldg(&s1[i]);
+  }
+  if (lane == 0 && p.row_token) p.row_token[row] = static_cast<int32_t>(t);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st) {
+  // the ticket and the block status words start at zero on every call
+  cudaError_t e = cudaMemsetAsync(p.ctrl, 0, sizeof(int) * (1 + p.nblk), st);
+  if (e != cudaSuccess) return e;
+  dispatch_kernel<<<p.nblk, NT, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherParams& p, cudaStream_t st) {
+  const long long total = static_cast<long long>(p.T) * p.k;
+  if (total == 0) return cudaSuccess;
+  const long long blocks = (total * 32 + 255) / 256;
+  const long long row_bytes = static_cast<long long>(p.d) * p.elem_bytes;
+  const bool vec16 = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(p.x_perm) % 16 == 0;
+  if (vec16)
+    gather_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, p.rows_alloc);
+  else
+    gather_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, p.rows_alloc);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,408 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Each expert e owns the rows [offsets[e], offsets[e+1]) of the expert-grouped
+// activations and computes, in nn.Linear layout (K contiguous for A and B):
+//   GELU   : h = gelu(A W1[e]^T + b1[e])                 -> bf16 [rows, F]
+//   SwiGLU : h = silu(A W1[e]^T) * (A W3[e]^T)           -> bf16 [rows, F]
+//   down   : y = h W2[e]^T + b2[e]                       -> fp32 [rows, d]
+// (the expert FFN of "Mixture-of-Experts Sparse Model Scaling", Core
+// Concepts: each expert is the dense FFN it replaces).
+//
+// Kernel design (one persistent CTA per SM, 256 threads):
+//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
+//               swizzle, 4-stage mbarrier ring (48 KB per stage)
+//   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16,
+//               fp32 accumulator in TMEM; tcgen05.commit frees smem stages
+//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators,
+//               so the epilogue of one tile overlaps the mainloop of the next)
+//   warps 4-7   epilogue: tcgen05.ld 32 columns at a time, fused activation,
+//               bias, conversion, row-masked 16-byte stores
+// SwiGLU puts 128 rows of W1 and the matching 128 rows of W3 into one
+// 256-row B tile, so one accumulator holds gate | up and the epilogue emits
+// 128 columns of h.  Tiles are ordered expert-major, then N, then M, so CTAs
+// running side by side share weight panels in L2.  Every barrier wait is
+// bounded; on expiry the CTA records MOE_ERR_DEVICE_TIMEOUT, drains its own
+// copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;
+constexpr int NTHREADS = 256;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers etc*/ +
+                           2 * (kMaxExperts + 1) * 4;
+
+enum { MODE_GELU = 0, MODE_SWIGLU = 1, MODE_DOWN = 2 };
+
+struct GemmArgs {
+  const int32_t* offsets;
+  int E;
+  int N_out;      // output columns
+  int N_w;        // weight rows per expert in the B tensor
+  int K;          // reduction length (multiple of 64)
+  int n_tiles;    // N tiles per expert
+  void* out;      // bf16 h or fp32 y
+  long long out_ld;
+  const float* bias;  // [E, N_out] or null
+  int* err;
+};
+
+__device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+
+struct TileInfo {
+  int e, row0, rows_valid, n0;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmB3, GemmArgs g) {
+  constexpr int BN_OUT = MODE == MODE_SWIGLU ? 128 : 256;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte align the tile ring (128-byte swizzle atoms)
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* tiles = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                 // [STAGES]
+  uint64_t* empty = bars + STAGES;       // [STAGES]
+  uint64_t* tfull = bars + 2 * STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;          // [2]
+  uint64_t* drain = tempty + 2;          // [1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
+  int* s_tstart = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);  // [E+1]
+  int* s_mt = s_tstart + kMaxExperts + 1;                                        // [E]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = g.E;
+
+  // ---- per-expert tile counts from the segment offsets
+  for (int e = tid; e < E; e += NTHREADS) {
+    const int cnt = g.offsets[e + 1] - g.offsets[e];
+    s_mt[e] = cnt > 0 ? (cnt + BM - 1) / BM : 0;
+  }
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if (MODE == MODE_SWIGLU) tma_prefetch_desc(&tmB3);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_tstart[e] = acc;
+      acc += s_mt[e] * g.n_tiles;
+    }
+    s_tstart[E] = acc;
+    *s_total = acc;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = *s_total;
+  const int KB = g.K / BK;
+
+  auto decode = [&](int tile, int& ecur, TileInfo& ti) {
+    while (s_tstart[ecur + 1] <= tile) ++ecur;
+    const int local = tile - s_tstart[ecur];
+    const int mt = s_mt[ecur];
+    const int nb = local / mt, mb = local - nb * mt;
+    const int seg0 = g.offsets[ecur];
+    const int cnt = g.offsets[ecur + 1] - seg0;
+    ti.e = ecur;
+    ti.row0 = seg0 + mb * BM;
+    ti.rows_valid = min(BM, cnt - mb * BM);
+    ti.n0 = nb * BN_OUT;
+  };
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_phase = 0;  // per-stage bit masks, for the drain
+      int ecur = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        TileInfo ti;
+        decode(tile, ecur, ti);
+        const int brow = ti.e * g.N_w + ti.n0;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, g.err, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
+          if (MODE == MODE_SWIGLU) {
+            tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+            tma_load_2d(sb + B_BYTES / 2, &tmB3, fb, kb * BK, brow);
+          } else {
+            tma_load_2d(sb, &tmB, fb, kb * BK, brow);
+          }
+          issued |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // make sure no copy into this CTA's shared memory is still in flight
+      for (int s = 0; s < STAGES; ++s)
+        if (issued >> s & 1u) mbar_wait_bounded(smem_u32(&full[s]), (last_phase >> s) & 1u, g.err, nullptr);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      bool ok = true;
+      bool any = false;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aphase ^ 1u, g.err, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, g.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sb);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // step 16 bf16 = 32 bytes along K inside the swizzled 128-byte rows
+            umma_bf16(dt, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), IDESC,
+                      (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&empty[stage]));
+          any = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[acc]));
+        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+      }
+      if (any) {
+        // every MMA issued by this thread has finished before TMEM is freed
+        umma_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, g.err, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ================= epilogue =================
+    const int q = warp - 4;                 // TMEM lane quarter
+    const int rloc = q * 32 + lane;         // row inside the tile
+    int acc = 0;
+    uint32_t aphase = 0;
+    int ecur = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      TileInfo ti;
+      decode(tile, ecur, ti);
+      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), aphase, g.err, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const bool row_ok = rloc < ti.rows_valid;
+      const long long row = static_cast<long long>(ti.row0) + rloc;
+      if constexpr (MODE == MODE_SWIGLU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+#pragma unroll 1
+        for (int c = 0; c < BN_OUT / 32; ++c) {
+          float gv[32], uv[32];
+          tmem_ld32(tbase + c * 32, gv);
+          tmem_ld32(tbase + 128 + c * 32, uv);
+          const int col = ti.n0 + c * 32;
+          if (row_ok && col < g.N_out) {
+            uint4 pk[4];
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              h2[i] = __floats2bfloat162_rn(silu_f(gv[2 * i]) * uv[2 * i], silu_f(gv[2 * i + 1]) * uv[2 * i + 1]);
+            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+          }
+        }
+      } else if constexpr (MODE == MODE_GELU) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+#pragma unroll 1
+        for (int c = 0; c < BN_OUT / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int col = ti.n0 + c * 32;
+          if (row_ok && col < g.N_out) {
+            const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
+            uint4 pk[4];
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a0 = v[2 * i], a1 = v[2 * i + 1];
+              if (bias) { a0 += bias[2 * i]; a1 += bias[2 * i + 1]; }
+              h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+          }
+        }
+      } else {
+        float* out = static_cast<float*>(g.out);
+#pragma unroll 1
+        for (int c = 0; c < BN_OUT / 32; ++c) {
+          float v[32];
+          tmem_ld32(tbase + c * 32, v);
+          const int col = ti.n0 + c * 32;
+          if (row_ok && col < g.N_out) {
+            const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
+            float4* dst = reinterpret_cast<float4*>(out + row * g.out_ld + col);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              if (bias) { o.x += bias[4 * i]; o.y += bias[4 * i + 1]; o.z += bias[4 * i + 2]; o.w += bias[4 * i + 3]; }
+              dst[i] = o;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (++acc == 2) { acc = 0; aphase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      g_encode_err = e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+      return;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode_err;
+}
+
+// 2-D bf16 tensor [rows, K] (K contiguous) read in boxes of box_rows x 64.
+cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const GemmArgs& g,
+                        long long rows_bound, int num_sms, cudaStream_t st) {
+  auto kern = grouped_gemm_kernel<MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  // upper bound on tiles: every expert may add one partial M tile
+  const long long mt_bound = (rows_bound + BM - 1) / BM + g.E;
+  const long long tiles_bound = mt_bound * g.n_tiles;
+  const int grid = static_cast<int>(std::min<long long>(num_sms, std::max<long long>(1, tiles_bound)));
+  kern<<<grid, NTHREADS, SMEM_BYTES, st>>>(a, b, b3, g);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t between_gemms) {
+  if (p.rows == 0) return cudaSuccess;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+
+  const bool swiglu = p.act == MOE_ACT_SWIGLU;
+  CUtensorMap mA1, mB1, mB3, mA2, mB2;
+  if ((e = make_map(&mA1, p.x_perm, p.rows, p.d, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mB1, p.W1, static_cast<long long>(p.E) * p.F, p.d, swiglu ? BN / 2 : BN)) != cudaSuccess) return e;
+  if (swiglu) {
+    if ((e = make_map(&mB3, p.W3, static_cast<long long>(p.E) * p.F, p.d, BN / 2)) != cudaSuccess) return e;
+  } else {
+    mB3 = mB1;
+  }
+  if ((e = make_map(&mA2, p.h, p.rows, p.F, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mB2, p.W2, static_cast<long long>(p.E) * p.d, p.F, BN)) != cudaSuccess) return e;
+
+  GemmArgs g1{};
+  g1.offsets = p.offsets;
+  g1.E = p.E;
+  g1.N_out = p.F;
+  g1.N_w = p.F;
+  g1.K = p.d;
+  g1.n_tiles = (p.F + (swiglu ? 127 : 255)) / (swiglu ? 128 : 256);
+  g1.out = p.h;
+  g1.out_ld = p.F;
+  g1.bias = swiglu ? nullptr : p.b1;
+  g1.err = p.err;
+  e = swiglu ? launch_mode<MODE_SWIGLU>(mA1, mB1, mB3, g1, p.rows, sms, st)
+             : launch_mode<MODE_GELU>(mA1, mB1, mB3, g1, p.rows, sms, st);
+  if (e != cudaSuccess) return e;
+  if (between_gemms != nullptr && (e = cudaEventRecord(between_gemms, st)) != cudaSuccess) return e;
+
+  GemmArgs g2{};
+  g2.offsets = p.offsets;
+  g2.E = p.E;
+  g2.N_out = p.d;
+  g2.N_w = p.d;
+  g2.K = p.F;
+  g2.n_tiles = (p.d + 255) / 256;
+  g2.out = p.y_perm;
+  g2.out_ld = p.d;
+  g2.bias = p.b2;
+  g2.err = p.err;
+  return launch_mode<MODE_DOWN>(mA2, mB2, mB2, g2, p.rows, sms, st);
+}
+
+}  // namespace moe

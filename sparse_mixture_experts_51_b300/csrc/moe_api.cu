@@ -1,0 +1,411 @@
+// C ABI of the MoE layer library: argument checks, workspace carve-up and
+// the launch sequence router -> dispatch -> gather -> expert GEMMs -> combine.
+// Declarations and the full contract are in include/moe_b300.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "moe_b300.h"
+#include "moe_b300_testing.h"
+
+namespace moe {
+
+namespace {
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+size_t dtype_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
+  WsLayout L{};
+  const long long Tk = s.T * s.k;
+  const long long EC = static_cast<long long>(s.E) * C;
+  L.rows = Tk < EC ? Tk : EC;
+  L.nblk_dispatch = static_cast<int>(Tk == 0 ? 1 : (Tk + kDispatchTile - 1) / kDispatchTile);
+  const size_t b = dtype_bytes(s.dtype);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  L.err = take(sizeof(int));
+  L.disp_ctrl = take(sizeof(int) * (1 + L.nblk_dispatch));
+  L.disp_agg = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
+  L.disp_incl = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
+  L.idx = take(sizeof(int32_t) * Tk);
+  L.w = take(sizeof(float) * Tk);
+  L.pos = take(sizeof(int32_t) * Tk);
+  L.counts = take(sizeof(int32_t) * s.E);
+  L.offsets = take(sizeof(int32_t) * (s.E + 1));
+  L.dropped = take(sizeof(long long));
+  L.x_perm = take(b * static_cast<size_t>(L.rows) * s.d);
+  L.h = take(b * static_cast<size_t>(L.rows) * s.d_ff);
+  L.y_perm = take(sizeof(float) * static_cast<size_t>(L.rows) * s.d);
+  L.total = o;
+  return L;
+}
+
+namespace {
+
+moe_status_t check_shape(const moe_shape_t* s) {
+  if (s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (s->T < 0 || s->d < 1 || s->E < 1 || s->k < 1 || s->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (s->k > s->E) return MOE_ERR_INVALID_ARG;
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (s->act != MOE_ACT_GELU && s->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (s->T * static_cast<long long>(s->k) >= (1LL << 31)) return MOE_ERR_UNSUPPORTED;
+  if (s->E > kMaxExperts || s->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  if (s->dtype == MOE_BF16 && (s->d % 64 != 0 || s->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
+  if (s->dtype == MOE_F32 && s->d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_shape_t* s, int32_t C, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOE_ERR_WORKSPACE;
+  if (ws_bytes < ws_layout(*s, C).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_capacity(int64_t T, int32_t k, int32_t E, double capacity_factor) {
+  if (T < 0 || k < 1 || E < 1 || !std::isfinite(capacity_factor) || capacity_factor <= 0.0) return -1;
+  const double v = std::ceil(capacity_factor * static_cast<double>(T) * static_cast<double>(k) / static_cast<double>(E));
+  if (!(v <= 2147483647.0)) return -1;
+  return static_cast<int32_t>(v);
+}
+
+int64_t moe_max_rows(const moe_shape_t* shape, int32_t C) {
+  if (check_shape(shape) == MOE_ERR_INVALID_ARG || C < 0) return -1;
+  const long long Tk = shape->T * shape->k;
+  const long long EC = static_cast<long long>(shape->E) * C;
+  return Tk < EC ? Tk : EC;
+}
+
+moe_status_t moe_workspace_size(const moe_shape_t* shape, int32_t C, size_t* bytes) {
+  if (bytes == nullptr || C < 0) return MOE_ERR_INVALID_ARG;
+  const moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  *bytes = ws_layout(*shape, C).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g, const float* b_g,
+                       const float* W_noise, const float* eps, int32_t* idx, float* w, float* logits,
+                       int64_t* stats, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->T > 0 && (x == nullptr || idx == nullptr || w == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (W_g == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((W_noise == nullptr) != (eps == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && !aligned16(x)) return MOE_ERR_UNSUPPORTED;
+  RouterParams p{};
+  p.x = x;
+  p.W_g = W_g;
+  p.b_g = b_g;
+  p.W_n = W_noise;
+  p.eps = eps;
+  p.T = static_cast<int>(shape->T);
+  p.d = shape->d;
+  p.E = shape->E;
+  p.k = shape->k;
+  p.idx = idx;
+  p.w = w;
+  p.logits = logits;
+  p.stats = reinterpret_cast<long long*>(stats);
+  p.err = nullptr;
+  return cuda_status(launch_router(p, shape->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x,
+                                  int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
+                                  void* x_perm, int32_t* row_token, void* ws, const WsLayout& L,
+                                  cudaStream_t st, int stall_block = -1) {
+  DispatchParams dp{};
+  dp.idx = idx;
+  dp.T = static_cast<int>(shape->T);
+  dp.k = shape->k;
+  dp.E = shape->E;
+  dp.C = C;
+  dp.pos = pos;
+  dp.counts = counts;
+  dp.offsets = offsets;
+  dp.dropped = reinterpret_cast<long long*>(dropped);
+  dp.ctrl = at<int>(ws, L.disp_ctrl);
+  dp.agg = at<int>(ws, L.disp_agg);
+  dp.incl = at<int>(ws, L.disp_incl);
+  dp.nblk = L.nblk_dispatch;
+  dp.stall_block = stall_block;
+  dp.err = at<int>(ws, L.err);
+  cudaError_t e = launch_dispatch(dp, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  GatherParams gp{};
+  gp.x = x;
+  gp.idx = idx;
+  gp.pos = pos;
+  gp.offsets = offsets;
+  gp.T = static_cast<int>(shape->T);
+  gp.k = shape->k;
+  gp.d = shape->d;
+  gp.E = shape->E;
+  gp.x_perm = x_perm;
+  gp.row_token = row_token;
+  gp.elem_bytes = static_cast<int>(dtype_bytes(shape->dtype));
+  gp.rows_alloc = L.rows;
+  gp.err = at<int>(ws, L.err);
+  return cuda_status(launch_gather(gp, st));
+}
+
+moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x, int32_t* pos,
+                          int32_t* counts, int32_t* offsets, int64_t* dropped, void* x_perm, int32_t* row_token,
+                          void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  if (counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, C);
+  if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
+  return dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, x_perm, row_token, ws, L,
+                       static_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_testing_dispatch_stalled(const moe_shape_t* shape, int32_t C, const int32_t* idx,
+                                          const void* x, int32_t* pos, int32_t* counts, int32_t* offsets,
+                                          int64_t* dropped, void* x_perm, int32_t stalled_tile, void* ws,
+                                          size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (C < 0 || counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, C);
+  if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  if (stalled_tile < 0 || stalled_tile >= L.nblk_dispatch) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
+  return dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, x_perm, nullptr, ws, L,
+                       static_cast<cudaStream_t>(stream), stalled_tile);
+}
+
+static moe_status_t ffn_impl(const moe_shape_t* shape, const void* x_perm, const int32_t* offsets, const void* W1,
+                             const void* W3, const void* W2, const float* b1, const float* b2, float* y_perm,
+                             void* ws, const WsLayout& L, cudaStream_t st) {
+  FfnParams fp{};
+  fp.x_perm = x_perm;
+  fp.offsets = offsets;
+  fp.W1 = W1;
+  fp.W3 = W3;
+  fp.W2 = W2;
+  fp.b1 = b1;
+  fp.b2 = b2;
+  fp.h = at<void>(ws, L.h);
+  fp.y_perm = y_perm;
+  fp.E = shape->E;
+  fp.d = shape->d;
+  fp.F = shape->d_ff;
+  fp.act = shape->act;
+  fp.rows = L.rows;
+  fp.err = at<int>(ws, L.err);
+  return cuda_status(shape->dtype == MOE_BF16 ? launch_ffn_bf16(fp, st) : launch_ffn_f32(fp, st));
+}
+
+static moe_status_t check_experts(const moe_shape_t* shape, const void* W1, const void* W3, const void* W2,
+                                  const float* b1) {
+  if (W1 == nullptr || W2 == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->act == MOE_ACT_SWIGLU && (W3 == nullptr || b1 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->act == MOE_ACT_GELU && W3 != nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(W1) || !aligned16(W2) || (W3 && !aligned16(W3))) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const void* x_perm, const int32_t* offsets,
+                            const void* W1, const void* W3, const void* W2, const float* b1, const float* b2,
+                            float* y_perm, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (C < 0 || offsets == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((st = check_experts(shape, W1, W3, W2, b1)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*shape, C);
+  if (L.rows > 0 && (x_perm == nullptr || y_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (L.rows > 0 && (!aligned16(x_perm) || !aligned16(y_perm))) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
+  return ffn_impl(shape, x_perm, offsets, W1, W3, W2, b1, b2, y_perm, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+static moe_status_t combine_impl(const moe_shape_t* shape, long long rows, const float* y_perm, const int32_t* idx,
+                                 const float* w, const int32_t* pos, const int32_t* offsets, const void* residual,
+                                 void* out, float* moe_out, int* err, cudaStream_t st) {
+  CombineParams cp{};
+  cp.y_perm = y_perm;
+  cp.idx = idx;
+  cp.w = w;
+  cp.pos = pos;
+  cp.offsets = offsets;
+  cp.residual = residual;
+  cp.out = out;
+  cp.moe_out = moe_out;
+  cp.T = static_cast<int>(shape->T);
+  cp.k = shape->k;
+  cp.d = shape->d;
+  cp.E = shape->E;
+  cp.rows = rows;
+  cp.dtype = shape->dtype;
+  cp.err = err;
+  return cuda_status(launch_combine(cp, st));
+}
+
+moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_perm, const int32_t* idx,
+                         const float* w, const int32_t* pos, const int32_t* offsets, const void* residual, void* out,
+                         float* moe_out, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (C < 0) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (idx == nullptr || w == nullptr || pos == nullptr || offsets == nullptr || out == nullptr))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, C);
+  if (L.rows > 0 && y_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!aligned16(out) || (residual && !aligned16(residual)) || (moe_out && !aligned16(moe_out)) ||
+                       (y_perm && !aligned16(y_perm))))
+    return MOE_ERR_UNSUPPORTED;
+  return combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, residual, out, moe_out, nullptr,
+                      static_cast<cudaStream_t>(stream));
+}
+
+static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
+                                 const void* x, const float* W_g, const float* b_g, const float* W_noise,
+                                 const float* eps, const void* W1, const void* W3, const void* W2, const float* b1,
+                                 const float* b2, void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
+                                 int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats, void* ws,
+                                 size_t ws_bytes, void* stream, void* const* stage_events) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  int32_t C = C_override;
+  if (C < 0) {
+    C = moe_capacity(shape->T, shape->k, shape->E, capacity_factor);
+    if (C < 0) return MOE_ERR_INVALID_ARG;
+  }
+  if (W_g == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((W_noise == nullptr) != (eps == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (x == nullptr || out == nullptr)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_experts(shape, W1, W3, W2, b1)) != MOE_OK) return st;
+  if (shape->T > 0 && (!aligned16(x) || !aligned16(out) || (moe_out && !aligned16(moe_out))))
+    return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
+  if (stage_events != nullptr) {
+    for (int i = 0; i < 6; ++i)
+      if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
+  }
+
+  const WsLayout L = ws_layout(*shape, C);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) -> moe_status_t {
+    if (stage_events == nullptr) return MOE_OK;
+    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s));
+  };
+  if (idx == nullptr) idx = at<int32_t>(ws, L.idx);
+  if (w == nullptr) w = at<float>(ws, L.w);
+  if (pos == nullptr) pos = at<int32_t>(ws, L.pos);
+  if (counts == nullptr) counts = at<int32_t>(ws, L.counts);
+  if (offsets == nullptr) offsets = at<int32_t>(ws, L.offsets);
+  if (dropped == nullptr) dropped = at<int64_t>(ws, L.dropped);
+
+  if ((st = mark(0)) != MOE_OK) return st;
+  if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, nullptr, stats, stream)) != MOE_OK) return st;
+  if ((st = mark(1)) != MOE_OK) return st;
+  if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
+                          s)) != MOE_OK)
+    return st;
+  if ((st = mark(2)) != MOE_OK) return st;
+  float* y_perm = at<float>(ws, L.y_perm);
+  FfnParams fp{};
+  fp.x_perm = at<void>(ws, L.x_perm);
+  fp.offsets = offsets;
+  fp.W1 = W1;
+  fp.W3 = W3;
+  fp.W2 = W2;
+  fp.b1 = b1;
+  fp.b2 = b2;
+  fp.h = at<void>(ws, L.h);
+  fp.y_perm = y_perm;
+  fp.E = shape->E;
+  fp.d = shape->d;
+  fp.F = shape->d_ff;
+  fp.act = shape->act;
+  fp.rows = L.rows;
+  fp.err = at<int>(ws, L.err);
+  if (shape->dtype == MOE_BF16) {
+    if ((st = cuda_status(launch_ffn_bf16(fp, s, stage_events ? static_cast<cudaEvent_t>(stage_events[3]) : nullptr))) != MOE_OK)
+      return st;
+  } else {
+    if ((st = cuda_status(launch_ffn_f32(fp, s))) != MOE_OK) return st;
+    if ((st = mark(3)) != MOE_OK) return st;
+  }
+  if ((st = mark(4)) != MOE_OK) return st;
+  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, out, moe_out, at<int>(ws, L.err), s)) !=
+      MOE_OK)
+    return st;
+  return mark(5);
+}
+
+moe_status_t moe_forward(const moe_shape_t* shape, double capacity_factor, int32_t C_override, const void* x,
+                         const float* W_g, const float* b_g, const float* W_noise, const float* eps, const void* W1,
+                         const void* W3, const void* W2, const float* b1, const float* b2, void* out, float* moe_out,
+                         int32_t* idx, float* w, int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
+                         int64_t* stats, void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
+                      moe_out, idx, w, pos, counts, offsets, dropped, stats, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity_factor, int32_t C_override, const void* x,
+                               const float* W_g, const float* b_g, const float* W_noise, const float* eps,
+                               const void* W1, const void* W3, const void* W2, const float* b1, const float* b2,
+                               void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos, int32_t* counts,
+                               int32_t* offsets, int64_t* dropped, int64_t* stats, void* ws, size_t ws_bytes,
+                               void* stream, void* const* stage_events) {
+  if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
+  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
+                      moe_out, idx, w, pos, counts, offsets, dropped, stats, ws, ws_bytes, stream, stage_events);
+}
+
+moe_status_t moe_get_device_error(void* ws, void* stream) {
+  if (ws == nullptr) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int code = 0;
+  if (cudaMemcpy(&code, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (code != 0) {
+    if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(code);
+}
+
+const char* moe_status_string(moe_status_t status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: valid but outside the supported set";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA runtime call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+    case MOE_ERR_BOUNDS: return "MOE_ERR_BOUNDS: a device-side index check failed";
+  }
+  return "unknown moe_status_t";
+}
+
+}  // extern "C"

@@ -1,0 +1,154 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments on the host before anything reaches a GPU.  CPU only:
+no call here launches a kernel (fake device pointers are never dereferenced
+because validation fails first)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from sparse_mixture_experts_51_b300 import _lib
+from sparse_mixture_experts_51_b300._lib import MoeShape
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+INC = os.path.join(ROOT, "include")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+FAKE = 0x7f0000000000  # 256-byte aligned, never dereferenced
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(INC):
+        if f.endswith(".h"):
+            src = open(os.path.join(INC, f)).read()
+            names |= set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _lib.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+    # and the binding knows every declared signature
+    assert names <= set(_lib.SIGNATURES) | {n for n in names if n.startswith("moe_testing_")}
+
+
+def test_capacity(lib):
+    assert lib.moe_capacity(64, 2, 4, 1.25) == 40
+    assert lib.moe_capacity(4096, 2, 8, 1.25) == 1280
+    assert lib.moe_capacity(16384, 2, 8, 4.0) == 16384
+    assert lib.moe_capacity(32768, 1, 64, 1.0) == 512
+    assert lib.moe_capacity(128, 6, 64, 2.0) == 24
+    assert lib.moe_capacity(8, 1, 4, 1.0) == 2
+    assert lib.moe_capacity(10, 1, 3, 1.0) == 4   # ceil(10/3)
+    assert lib.moe_capacity(0, 1, 3, 1.0) == 0
+    for bad in [(-1, 1, 4, 1.0), (8, 0, 4, 1.0), (8, 1, 0, 1.0), (8, 1, 4, 0.0), (8, 1, 4, float("nan")),
+                (8, 1, 4, float("inf")), (1 << 40, 16, 1, 1.0)]:
+        assert lib.moe_capacity(*bad) == -1, bad
+
+
+def _shape(**kw):
+    base = dict(T=64, d=64, E=4, k=2, d_ff=64, dtype=1, act=0)
+    base.update(kw)
+    return MoeShape(**base)
+
+
+def _ws(lib, shape, C):
+    n = ctypes.c_size_t(0)
+    st = lib.moe_workspace_size(ctypes.byref(shape), C, ctypes.byref(n))
+    return st, n.value
+
+
+def test_workspace_size_and_shape_validation(lib):
+    st, n = _ws(lib, _shape(), 40)
+    assert st == OK and n > 0 and n % 256 == 0
+    # grows with capacity-bounded rows
+    assert _ws(lib, _shape(), 80)[1] >= n
+    assert lib.moe_max_rows(ctypes.byref(_shape()), 40) == 128
+    assert lib.moe_max_rows(ctypes.byref(_shape()), 10) == 40
+    for kw, want in [(dict(T=-1), INVALID), (dict(d=0), INVALID), (dict(E=0), INVALID), (dict(k=0), INVALID),
+                     (dict(k=5), INVALID), (dict(d_ff=0), INVALID), (dict(dtype=7), INVALID), (dict(act=9), INVALID),
+                     (dict(E=129, k=2), UNSUPPORTED), (dict(E=32, k=17), UNSUPPORTED),
+                     (dict(d=96), UNSUPPORTED), (dict(d_ff=100), UNSUPPORTED), (dict(dtype=0, d=30), UNSUPPORTED),
+                     (dict(T=1 << 30, k=2), UNSUPPORTED)]:
+        assert _ws(lib, _shape(**kw), 40)[0] == want, kw
+    assert lib.moe_workspace_size(ctypes.byref(_shape()), -1, ctypes.byref(ctypes.c_size_t())) == INVALID
+    assert lib.moe_workspace_size(None, 4, ctypes.byref(ctypes.c_size_t())) == INVALID
+
+
+P = ctypes.c_void_p
+
+# The calls below pass fake device pointers that validation must reject before
+# any launch.  They only run where no GPU is visible, so a validation bug can
+# never turn into a kernel reading a bogus address.
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="fake-pointer checks run on CPU-only hosts")
+
+
+@no_gpu
+def test_route_argument_errors(lib):
+    s = _shape()
+    f = P(FAKE)
+    # missing W_g / idx / w
+    assert lib.moe_route(ctypes.byref(s), f, None, None, None, None, f, f, None, None, None) == INVALID
+    assert lib.moe_route(ctypes.byref(s), f, f, None, None, None, None, f, None, None, None) == INVALID
+    # noise needs both W_noise and eps
+    assert lib.moe_route(ctypes.byref(s), f, f, None, f, None, f, f, None, None, None) == INVALID
+    assert lib.moe_route(ctypes.byref(s), f, f, None, None, f, f, f, None, None, None) == INVALID
+    # misaligned tokens
+    assert lib.moe_route(ctypes.byref(s), P(FAKE + 2), f, None, None, None, f, f, None, None, None) == UNSUPPORTED
+
+
+@no_gpu
+def test_dispatch_ffn_combine_argument_errors(lib):
+    s = _shape()
+    f = P(FAKE)
+    st, n = _ws(lib, s, 40)
+    # dispatch: null outputs, negative C, small / misaligned workspace
+    assert lib.moe_dispatch(ctypes.byref(s), 40, f, f, f, None, f, f, f, None, f, n, None) == INVALID
+    assert lib.moe_dispatch(ctypes.byref(s), -2, f, f, f, f, f, f, f, None, f, n, None) == INVALID
+    assert lib.moe_dispatch(ctypes.byref(s), 40, f, f, f, f, f, f, f, None, f, n - 1, None) == WORKSPACE
+    assert lib.moe_dispatch(ctypes.byref(s), 40, f, f, f, f, f, f, f, None, P(FAKE + 16), n, None) == WORKSPACE
+    assert lib.moe_dispatch(ctypes.byref(s), 40, f, f, f, f, f, f, f, None, None, n, None) == WORKSPACE
+    # expert ffn: GELU takes no W3; SwiGLU needs W3 and no b1
+    sg = _shape(act=1)
+    assert lib.moe_expert_ffn(ctypes.byref(s), 40, f, f, f, f, f, None, None, f, f, n, None) == INVALID
+    assert lib.moe_expert_ffn(ctypes.byref(sg), 40, f, f, f, None, f, None, None, f, f, n, None) == INVALID
+    assert lib.moe_expert_ffn(ctypes.byref(sg), 40, f, f, f, f, f, f, None, f, f, n, None) == INVALID
+    assert lib.moe_expert_ffn(ctypes.byref(s), 40, f, f, P(FAKE + 8), None, f, None, None, f, f, n, None) == UNSUPPORTED
+    # combine: missing pieces
+    assert lib.moe_combine(ctypes.byref(s), 40, f, None, f, f, f, None, f, None, None) == INVALID
+    assert lib.moe_combine(ctypes.byref(s), 40, None, f, f, f, f, None, f, None, None) == INVALID
+
+
+@no_gpu
+def test_forward_argument_errors(lib):
+    s = _shape()
+    f = P(FAKE)
+    st, n = _ws(lib, s, 40)
+    args = [f, f, None, None, None, f, None, f, None, None, f, None, None, None, None, None, None, None, None]
+    # bad capacity factor with no override
+    assert lib.moe_forward(ctypes.byref(s), 0.0, -1, *args, f, n, None) == INVALID
+    # a workspace sized for C=10 (40 grouped rows) is too small for cf=1.25 (C=40, 128 rows)
+    st, n10 = _ws(lib, s, 10)
+    assert n10 < n
+    assert lib.moe_forward(ctypes.byref(s), 1.25, -1, *args, f, n10, None) == WORKSPACE
+    assert lib.moe_forward(ctypes.byref(s), 1.0, 40, *args, f, n10, None) == WORKSPACE
+    # missing output
+    bad = list(args)
+    bad[10] = None
+    assert lib.moe_forward(ctypes.byref(s), 1.25, -1, *bad, f, n, None) == INVALID
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.moe_status_string(code).decode().startswith(name)
+    assert b"unknown" in lib.moe_status_string(99)
