@@ -96,7 +96,7 @@ def test_steps(w):
 
 def test_route_near_tie_statistic():
     """Tokens whose k-th and (k+1)-th logits are within 1e-4 are counted."""
-    T, d, E = 64, 32, 4
+    T, d, E = 64, 64, 4
     x = torch.zeros(T, d, dtype=torch.bfloat16)
     x[:, 0] = 1.0
     Wg = torch.zeros(d, E)
