@@ -148,6 +148,33 @@ MOE_API moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int
                           int64_t* dropped, void* x_perm, int32_t* row_token,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* moe_dispatch for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a library-integration entry point, not a step
+ * of the method.  Some callers cannot allocate a workspace: a plug-in whose
+ * host framework owns all device memory and passes it only the operation's
+ * inputs and outputs, or a serving loop whose device memory plan is fixed up
+ * front and where cudaMalloc (which may synchronise the device) is not
+ * allowed.  This call computes exactly what moe_dispatch computes (same
+ * arguments and outputs, minus the workspace) and keeps its scan state in
+ * a fixed array in the library's own device global memory instead.
+ *   error_out  [1] int32 | NULL  device output: set to 0 at the start of the
+ *                                call, then to the first device-side error of
+ *                                the call (MOE_ERR_BOUNDS / _DEVICE_TIMEOUT)
+ * Limits: T*k <= 1048576 assignments (and E <= 128); larger sizes return
+ * MOE_ERR_UNSUPPORTED before anything is enqueued.  The array (about
+ * 257 KiB) stays resident on every GPU that loads the library until the
+ * process exits.  It allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library call.  The first call on a device, with that device
+ * current, looks up the array's device address (cudaGetSymbolAddress) and
+ * caches it; make that first call before any stream capture.  All calls
+ * share the one array and each call clears the parts that must start at
+ * zero: calls whose kernels may overlap on the GPU (unordered streams,
+ * several host threads) race on it and must be serialised by the caller. */
+MOE_API moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C, const int32_t* idx,
+                                          const void* x, int32_t* pos, int32_t* counts, int32_t* offsets,
+                                          int64_t* dropped, void* x_perm, int32_t* row_token,
+                                          int32_t* error_out, void* stream);
+
 /* Step 4: every expert's FFN over its segment of the expert-grouped rows.
  *   x_perm   [moe_max_rows,d]  dtype   grouped rows (moe_dispatch)
  *   offsets  [E+1] int32               segment starts (moe_dispatch)

@@ -39,6 +39,7 @@ SIGNATURES = {
     "moe_route": (ctypes.c_int, [_SHAPE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
+    "moe_dispatch_noalloc": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 10),
     "moe_expert_ffn": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),

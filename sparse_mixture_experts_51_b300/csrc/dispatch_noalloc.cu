@@ -1,0 +1,130 @@
+// moe_dispatch_noalloc: capacity-limited dispatch + gather for callers that
+// cannot allocate device memory.
+//
+// moe_dispatch keeps the state of its cross-block scan (tile ticket, per-tile
+// status flags, per-tile expert histograms and prefixes) in a workspace the
+// caller allocates.  Some callers cannot provide one: a plug-in whose host
+// framework owns all device memory and hands it only the operation's inputs
+// and outputs, or a latency-critical serving loop whose device memory plan is
+// fixed up front and where a cudaMalloc (which may synchronise the device) is
+// not allowed on the request path.  This entry point keeps that scan state in
+// a fixed-size array in device global memory that belongs to the library
+// itself, so it needs no allocation at all.
+//
+// The array (g_dispatch_scratch) is sized for at most kNoAllocMaxAssignments
+// = 1,048,576 assignments (T*k), i.e. 256 dispatch tiles, and E <= 128:
+// about 257 KiB, held by every GPU that loads the library until the process
+// exits.  Every call shares it: the tile ticket and status flags are cleared
+// at the start of each call (they must start at zero; the histogram and
+// prefix slots are always written before they are read), and calls whose
+// kernels overlap on the GPU (different streams without ordering, or
+// several host threads) race on it and must be serialised by the caller.
+//
+// Host code cannot use the array's name as a device address, so the first
+// call on each device (with that device current) looks the address up with
+// cudaGetSymbolAddress and caches it; later calls on that device reuse it.
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "moe_b300.h"
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxTiles = 256;
+constexpr long long kNoAllocMaxAssignments = static_cast<long long>(kNoAllocMaxTiles) * kDispatchTile;
+// layout in ints: [0] ticket, [1, 1+kNoAllocMaxTiles) tile status,
+// then per-tile expert histograms [tiles][E], then inclusive prefixes [tiles][E]
+constexpr size_t kCtrlInts = 1 + kNoAllocMaxTiles;
+constexpr size_t kAggOffset = (kCtrlInts + 63) / 64 * 64;
+constexpr size_t kInclOffset = kAggOffset + static_cast<size_t>(kNoAllocMaxTiles) * kMaxExperts;
+constexpr size_t kScratchInts = kInclOffset + static_cast<size_t>(kNoAllocMaxTiles) * kMaxExperts;
+
+static __device__ __align__(256) int g_dispatch_scratch[kScratchInts];
+
+constexpr int kMaxCachedDevices = 64;
+std::mutex g_scratch_mu;
+int* g_scratch_ptr[kMaxCachedDevices] = {};
+
+// Device address of g_dispatch_scratch on the current device (looked up once per device).
+cudaError_t scratch_on_current_device(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (dev >= 0 && dev < kMaxCachedDevices && g_scratch_ptr[dev] != nullptr) {
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxCachedDevices) g_scratch_ptr[dev] = static_cast<int*>(p);
+  *out = static_cast<int*>(p);
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C, const int32_t* idx,
+                                             const void* x, int32_t* pos, int32_t* counts, int32_t* offsets,
+                                             int64_t* dropped, void* x_perm, int32_t* row_token,
+                                             int32_t* error_out, void* stream) {
+  if (shape == nullptr || C < 0) return MOE_ERR_INVALID_ARG;
+  if (shape->T < 0 || shape->d < 1 || shape->E < 1 || shape->k < 1 || shape->k > shape->E ||
+      shape->d_ff < 1 || (shape->dtype != MOE_F32 && shape->dtype != MOE_BF16) ||
+      (shape->act != MOE_ACT_GELU && shape->act != MOE_ACT_SWIGLU))
+    return MOE_ERR_INVALID_ARG;
+  if (shape->E > kMaxExperts || shape->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
+  const long long Tk = shape->T * static_cast<long long>(shape->k);
+  if (Tk > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array
+  if (counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
+  const long long EC = static_cast<long long>(shape->E) * C;
+  const long long rows = Tk < EC ? Tk : EC;
+  if (rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+
+  int* scratch = nullptr;
+  if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (error_out != nullptr && cudaMemsetAsync(error_out, 0, sizeof(int32_t), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  DispatchParams dp{};
+  dp.idx = idx;
+  dp.T = static_cast<int>(shape->T);
+  dp.k = shape->k;
+  dp.E = shape->E;
+  dp.C = C;
+  dp.pos = pos;
+  dp.counts = counts;
+  dp.offsets = offsets;
+  dp.dropped = reinterpret_cast<long long*>(dropped);
+  dp.ctrl = scratch;  // launch_dispatch clears the ticket and the status flags
+  dp.agg = scratch + kAggOffset;
+  dp.incl = scratch + kInclOffset;
+  dp.nblk = static_cast<int>(Tk == 0 ? 1 : (Tk + kDispatchTile - 1) / kDispatchTile);
+  dp.stall_block = -1;
+  dp.err = error_out;
+  if (launch_dispatch(dp, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GatherParams gp{};
+  gp.x = x;
+  gp.idx = idx;
+  gp.pos = pos;
+  gp.offsets = offsets;
+  gp.T = static_cast<int>(shape->T);
+  gp.k = shape->k;
+  gp.d = shape->d;
+  gp.E = shape->E;
+  gp.x_perm = x_perm;
+  gp.row_token = row_token;
+  gp.elem_bytes = shape->dtype == MOE_BF16 ? 2 : 4;
+  gp.rows_alloc = rows;
+  gp.err = error_out;
+  return launch_gather(gp, st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
