@@ -46,7 +46,7 @@ GEMM_SOURCES = ["sparse_mixture_experts_51_b300/csrc/gemm_tc.cu", "sparse_mixtur
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -90,16 +90,22 @@ def gemm1_work(w, counts):
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs: through NVML when it loads, else by polling nvidia-smi."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
                0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
                0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,clocks_event_reasons.gpu_idle,"
+                  "clocks_event_reasons.sw_power_cap,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown")
 
     def __init__(self, index: int, period_s: float = 0.01):
-        self.samples = []
+        self.index = index
+        self.samples = []  # (mhz, reason bits)
         self.max_mhz = None
-        self.ok = False
+        self.mode = None
+        self.err = ""
         self._stop = threading.Event()
         self.period = period_s
         try:
@@ -108,39 +114,60 @@ class ClockSampler:
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # NVML missing: report it rather than guess
+            self.mode = "nvml"
+        except Exception as e:
             self.err = repr(e)
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _reasons(self):
+    def _run_nvml(self):
         nv = self.nv
         fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
-        return fn(self.h)
-
-    def _run(self):
         while not self._stop.is_set():
             try:
-                mhz = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
-                util = self.nv.nvmlDeviceGetUtilizationRates(self.h).gpu
-                self.samples.append((mhz, int(self._reasons()), util))
+                self.samples.append((nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM), int(fn(self.h))))
             except Exception:
                 pass
             time.sleep(self.period)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "nvidia-smi":
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            bits_of = [0x1, 0x4, 0x8, 0x40, 0x20]
+            for line in out.splitlines():
+                f = [v.strip() for v in line.split(",")]
+                if len(f) < 8:
+                    continue
+                try:
+                    mhz, mx = float(f[0]), float(f[1])
+                except ValueError:
+                    continue
+                bits = 0
+                for b, v in zip(bits_of, f[3:8]):
+                    if v.lower().startswith("active"):
+                        bits |= b
+                self.max_mhz = mx
+                self.samples.append((mhz, bits))
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "NVML unavailable"}
+        if self.mode is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no clock source: " + self.err}
         busy = [s for s in self.samples if not (s[1] & 0x1)] or self.samples
         mhz = [s[0] for s in busy]
         bits = 0
@@ -148,7 +175,7 @@ class ClockSampler:
             bits |= s[1]
         reasons = [name for bit, name in self.REASONS.items() if bits & bit and bit != 0x1]
         return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(busy)}
+                "reasons": reasons, "samples": len(busy), "source": self.mode}
 
 
 _ORACLE_CACHE = {}
