@@ -4,8 +4,9 @@
 // w[t,r] * y_perm[offsets[idx[t,r]] + pos[t,r]]  ("LLM part 09: Sparse
 // Mixture-of-Experts (MoE)", s1 output equation and s3 residual bypass of
 // dropped tokens; "Mixture-of-Experts Sparse Model Scaling", Lab 1 weighted
-// accumulation).  One warp per token gathers its k expert rows with 16-byte
-// loads and writes the token once: deterministic, no atomics.
+// accumulation).  Each thread owns 8 consecutive elements of one token,
+// gathers them from its k expert rows with 16-byte loads and writes them
+// once: deterministic, no atomics, HBM-bound.
 //
 // fp32 FFN: the grouped expert MLP on CUDA cores for fp32 layers (whose
 // tolerance rules out tf32/bf16 tensor cores): one warp per output element,
@@ -42,56 +43,95 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(h);
 }
 
+// One thread per (token, 8-element chunk): it resolves the token's kept
+// expert rows (k small loads, L1-resident across the token's chunks), issues
+// every 16-byte load of the chunk at once (k expert rows, the residual), and
+// writes the chunk once.  Ranks are summed in order 0..k-1 in fp32.
 template <typename TO>
-__global__ void __launch_bounds__(256) combine_kernel(CombineParams p) {
+__global__ void __launch_bounds__(256) combine_kernel(CombineParams p, long long items, int chunks) {
+  const long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (it >= items) return;
+  const long long t = it / chunks;
+  const int c = static_cast<int>(it - t * chunks) * 8;
+  const int k = p.k, d = p.d;
+  // the residual chunk first: its load overlaps the expert-row loads
+  const TO* res = static_cast<const TO*>(p.residual);
+  float r0[4] = {0.f, 0.f, 0.f, 0.f}, r1[4] = {0.f, 0.f, 0.f, 0.f};
+  if (res) {
+    load4<TO>(res + t * d + c, r0);
+    load4<TO>(res + t * d + c + 4, r1);
+  }
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int r = 0; r < k; ++r) {
+    const int ps = __ldg(p.pos + t * k + r);
+    if (ps < 0) continue;
+    const int e = __ldg(p.idx + t * k + r);
+    long long row = -1;
+    if (e >= 0 && e < p.E) row = static_cast<long long>(__ldg(p.offsets + e)) + ps;
+    if (row < 0 || row >= p.rows) {
+      record_error(p.err, MOE_ERR_BOUNDS);
+      continue;
+    }
+    const float wt = __ldg(p.w + t * k + r);
+    const float4* src = reinterpret_cast<const float4*>(p.y_perm + row * d + c);
+    const float4 a = __ldg(src), b = __ldg(src + 1);
+    acc[0] = fmaf(wt, a.x, acc[0]); acc[1] = fmaf(wt, a.y, acc[1]);
+    acc[2] = fmaf(wt, a.z, acc[2]); acc[3] = fmaf(wt, a.w, acc[3]);
+    acc[4] = fmaf(wt, b.x, acc[4]); acc[5] = fmaf(wt, b.y, acc[5]);
+    acc[6] = fmaf(wt, b.z, acc[6]); acc[7] = fmaf(wt, b.w, acc[7]);
+  }
+  if (p.moe_out) {
+    float4* mo = reinterpret_cast<float4*>(p.moe_out + t * d + c);
+    mo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    mo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  float o0[4], o1[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o0[i] = res ? r0[i] + acc[i] : acc[i];
+    o1[i] = res ? r1[i] + acc[4 + i] : acc[4 + i];
+  }
+  TO* out = static_cast<TO*>(p.out);
+  store4<TO>(out + t * d + c, o0);
+  store4<TO>(out + t * d + c + 4, o1);
+}
+
+// d not a multiple of 8 (fp32 layers with d % 4 == 0): one warp per token, 4 elements per lane.
+template <typename TO>
+__global__ void __launch_bounds__(256) combine_kernel4(CombineParams p) {
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= p.T) return;
   const int k = p.k, d = p.d;
-  long long row[kMaxTopK];
-  float wt[kMaxTopK];
-#pragma unroll
-  for (int r = 0; r < kMaxTopK; ++r) {
-    row[r] = -1;
-    wt[r] = 0.f;
-    if (r < k) {
-      const int ps = p.pos[t * k + r];
-      if (ps >= 0) {
-        const int e = p.idx[t * k + r];
-        long long rw = -1;
-        if (e >= 0 && e < p.E) rw = static_cast<long long>(p.offsets[e]) + ps;
-        if (rw < 0 || rw >= p.rows) {
-          if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
-          rw = -1;
-        }
-        row[r] = rw;
-        wt[r] = p.w[t * k + r];
-      }
-    }
-  }
-  const TO* res = static_cast<const TO*>(p.residual);
-  TO* out = static_cast<TO*>(p.out);
   for (int c = lane * 4; c < d; c += 128) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < kMaxTopK; ++r) {
-      if (r < k && row[r] >= 0) {
-        float y[4];
-        const float4 q = __ldg(reinterpret_cast<const float4*>(p.y_perm + row[r] * d + c));
-        y[0] = q.x; y[1] = q.y; y[2] = q.z; y[3] = q.w;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[i] = fmaf(wt[r], y[i], acc[i]);
+    for (int r = 0; r < k; ++r) {
+      const int ps = p.pos[t * k + r];
+      if (ps < 0) continue;
+      const int e = p.idx[t * k + r];
+      long long row = -1;
+      if (e >= 0 && e < p.E) row = static_cast<long long>(p.offsets[e]) + ps;
+      if (row < 0 || row >= p.rows) {
+        record_error(p.err, MOE_ERR_BOUNDS);
+        continue;
       }
+      const float wt = p.w[t * k + r];
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p.y_perm + row * d + c));
+      acc[0] = fmaf(wt, q.x, acc[0]); acc[1] = fmaf(wt, q.y, acc[1]);
+      acc[2] = fmaf(wt, q.z, acc[2]); acc[3] = fmaf(wt, q.w, acc[3]);
     }
     if (p.moe_out) store4<float>(p.moe_out + t * d + c, acc);
     float o[4] = {acc[0], acc[1], acc[2], acc[3]};
-    if (res) {
+    if (p.residual) {
       float rv[4];
-      load4<TO>(res + t * d + c, rv);
+      load4<TO>(static_cast<const TO*>(p.residual) + t * d + c, rv);
 #pragma unroll
       for (int i = 0; i < 4; ++i) o[i] = rv[i] + acc[i];
     }
-    store4<TO>(out + t * d + c, o);
+    store4<TO>(static_cast<TO*>(p.out) + t * d + c, o);
   }
 }
 
@@ -152,11 +192,21 @@ __global__ void __launch_bounds__(256) ffn2_f32_kernel(FfnParams p) {
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
-  const long long blocks = (static_cast<long long>(p.T) * 32 + 255) / 256;
-  if (p.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
-  else
-    combine_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  if (p.d % 8 == 0) {
+    const int chunks = p.d / 8;
+    const long long items = static_cast<long long>(p.T) * chunks;
+    const long long blocks = (items + 255) / 256;
+    if (p.dtype == MOE_BF16)
+      combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, items, chunks);
+    else
+      combine_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, items, chunks);
+  } else {
+    const long long blocks = (static_cast<long long>(p.T) * 32 + 255) / 256;
+    if (p.dtype == MOE_BF16)
+      combine_kernel4<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+    else
+      combine_kernel4<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -9,15 +9,19 @@
 // to the same expert, kept iff pos < C.
 //
 // Design.  One pass, deterministic, no atomics deciding any slot:
-//   * each block takes a tile of 4096 consecutive priority positions; a block
+//   * each block takes a tile of 256 x ITEMS consecutive priority positions
+//     (1024 for short batches, 4096 above 262144 assignments); a block
 //     obtains its tile index from a ticket counter, so a block only ever
 //     waits on blocks that are already running;
-//   * inside the tile, 16 steps of 256 assignments: warps rank equal experts
-//     with match.any + popc, a per-warp histogram in shared memory orders the
-//     warps, and a running per-expert count orders the steps;
-//   * the per-expert block totals are scanned across blocks with a
-//     decoupled look-back over E-wide descriptors (aggregate / inclusive
-//     prefix); every wait is bounded and records MOE_ERR_DEVICE_TIMEOUT;
+//   * all ITEMS expert ids of a thread are loaded at once; warps rank equal
+//     experts with match.any + popc, the per-(step, warp, expert) counts go
+//     to shared memory, and one per-expert exclusive scan over the
+//     (step, warp) sequence orders every assignment of the tile;
+//   * the per-expert tile totals are scanned across tiles with a decoupled
+//     look-back over E-wide descriptors (aggregate / inclusive prefix): one
+//     warp reads the flags of 32 predecessors at a time and sums their
+//     aggregates up to the nearest inclusive prefix; every wait is bounded
+//     and records MOE_ERR_DEVICE_TIMEOUT;
 //   * the block holding the last tile turns the loads into counts, segment
 //     offsets and the drop count.
 #include "common.cuh"
@@ -27,7 +31,6 @@ namespace moe {
 namespace {
 
 constexpr int NT = kDispatchThreads;
-constexpr int ITEMS = kDispatchItemsPerThread;
 constexpr int NWARP = NT / 32;
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -39,10 +42,12 @@ __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// dynamic shared memory: s_hist [ITEMS][NWARP][E] ints
+template <int ITEMS>
 __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
-  __shared__ int s_cnt[kMaxExperts];            // running count per expert in this tile
-  __shared__ int s_whist[NWARP][kMaxExperts];   // this step's count per warp and expert
-  __shared__ int s_excl[kMaxExperts];           // assignments to each expert before this tile
+  extern __shared__ int s_hist[];
+  __shared__ int s_tot[kMaxExperts];   // assignments to each expert inside this tile
+  __shared__ int s_excl[kMaxExperts];  // assignments to each expert before this tile
   __shared__ int s_ticket;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -50,15 +55,14 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
   const long long total = static_cast<long long>(p.T) * p.k;
 
   if (tid == 0) s_ticket = atomicAdd(&p.ctrl[0], 1);
-  for (int i = tid; i < kMaxExperts; i += NT) s_cnt[i] = 0;
-  for (int i = tid; i < NWARP * kMaxExperts; i += NT) (&s_whist[0][0])[i] = 0;
+  for (int i = tid; i < ITEMS * NWARP * E; i += NT) s_hist[i] = 0;
   __syncthreads();
   const int b = s_ticket;
   int* status = p.ctrl + 1;
   const long long base = static_cast<long long>(b) * (NT * ITEMS);
 
+  // ---- every expert id of this thread, loaded at once
   int my_e[ITEMS], my_rank[ITEMS];
-  const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const long long j = base + static_cast<long long>(i) * NT + tid;
@@ -66,42 +70,47 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
     if (j < total) {
       const int r = static_cast<int>(j / p.T);
       const int t = static_cast<int>(j - static_cast<long long>(r) * p.T);
-      e = p.idx[static_cast<long long>(t) * p.k + r];
-      if (e < 0 || e >= E) {
-        record_error(p.err, MOE_ERR_BOUNDS);
-        e = -1;
-      }
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank_in_warp = __popc(peers & lt_mask);
-    if (e >= 0 && rank_in_warp == 0) s_whist[warp][e] = __popc(peers);
-    __syncthreads();
-    int rank = 0;
-    if (e >= 0) {
-      rank = s_cnt[e] + rank_in_warp;
-      for (int w2 = 0; w2 < warp; ++w2) rank += s_whist[w2][e];
+      e = __ldg(p.idx + static_cast<long long>(t) * p.k + r);
     }
     my_e[i] = e;
-    my_rank[i] = rank;
-    __syncthreads();
-    for (int ex = tid; ex < E; ex += NT) {
-      int sum = 0;
-#pragma unroll
-      for (int w2 = 0; w2 < NWARP; ++w2) {
-        sum += s_whist[w2][ex];
-        s_whist[w2][ex] = 0;
-      }
-      s_cnt[ex] += sum;
-    }
-    __syncthreads();
   }
+  // ---- rank inside the warp step; per-(step, warp, expert) counts
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    int e = my_e[i];
+    const long long j = base + static_cast<long long>(i) * NT + tid;
+    if (j < total && (e < 0 || e >= E)) {  // an expert id out of range takes no slot
+      record_error(p.err, MOE_ERR_BOUNDS);
+      e = -1;
+    }
+    my_e[i] = e;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    my_rank[i] = __popc(peers & lt_mask);
+    if (e >= 0 && my_rank[i] == 0) s_hist[(i * NWARP + warp) * E + e] = __popc(peers);
+  }
+  __syncthreads();
+  // ---- per expert: exclusive scan over the (step, warp) sequence, in priority order
+  for (int ex = tid; ex < E; ex += NT) {
+    int run = 0;
+    for (int sw = 0; sw < ITEMS * NWARP; ++sw) {
+      const int c = s_hist[sw * E + ex];
+      s_hist[sw * E + ex] = run;
+      run += c;
+    }
+    s_tot[ex] = run;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i)
+    if (my_e[i] >= 0) my_rank[i] += s_hist[(i * NWARP + warp) * E + my_e[i]];
 
   // ---- publish this tile's per-expert totals, then look back for the prefix
   int* agg = p.agg + static_cast<long long>(b) * E;
   int* incl = p.incl + static_cast<long long>(b) * E;
   for (int ex = tid; ex < E; ex += NT) {
-    __stcg(&agg[ex], s_cnt[ex]);
-    if (b == 0) __stcg(&incl[ex], s_cnt[ex]);
+    __stcg(&agg[ex], s_tot[ex]);
+    if (b == 0) __stcg(&incl[ex], s_tot[ex]);
   }
   __threadfence();
   __syncthreads();
@@ -114,29 +123,41 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
     for (int s = 0; s < SL; ++s) ex_acc[s] = 0;
     int pred = b - 1;
     bool timed_out = false;
+    const unsigned long long t0 = globaltimer_ns();
     while (pred >= 0) {
-      int f = 0;
-      if (lane == 0) {
-        const unsigned long long t0 = globaltimer_ns();
-        unsigned spins = 0;
-        while ((f = ld_acquire(&status[pred])) == 0) {
-          if ((++spins & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) break;
+      // flags of the 32 predecessors pred, pred-1, ..., pred-31 (lane i: tile pred-i)
+      const int tile = pred - lane;
+      int f = 0, first_incl = 32;
+      unsigned spins = 0;
+      while (true) {
+        f = tile >= 0 ? ld_acquire(&status[tile]) : -1;
+        const unsigned incl_mask = __ballot_sync(0xffffffffu, f == 2);
+        const unsigned zero_mask = __ballot_sync(0xffffffffu, f == 0);
+        first_incl = incl_mask ? __ffs(incl_mask) - 1 : 32;
+        // usable once every tile up to the nearest inclusive prefix has published
+        const unsigned need = first_incl >= 31 ? 0xffffffffu : ((2u << first_incl) - 1u);
+        if ((zero_mask & need) == 0) break;
+        if ((++spins & 15u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+          timed_out = true;
+          break;
         }
       }
-      f = __shfl_sync(0xffffffffu, f, 0);
-      if (f == 0) {
-        timed_out = true;
-        break;
-      }
+      if (timed_out) break;
       __threadfence();
-      const int* src = (f == 2 ? p.incl : p.agg) + static_cast<long long>(pred) * E;
+      // aggregates of the tiles before the inclusive one, then its inclusive prefix
+      const int n_agg = min(first_incl, pred + 1);
 #pragma unroll
       for (int s = 0; s < SL; ++s) {
         const int ex = lane + 32 * s;
-        if (ex < E) ex_acc[s] += __ldcg(&src[ex]);
+        if (ex < E) {
+          int sum = 0;
+          for (int i2 = 0; i2 < n_agg; ++i2) sum += __ldcg(&p.agg[static_cast<long long>(pred - i2) * E + ex]);
+          if (first_incl < 32) sum += __ldcg(&p.incl[static_cast<long long>(pred - first_incl) * E + ex]);
+          ex_acc[s] += sum;
+        }
       }
-      if (f == 2) break;
-      --pred;
+      if (first_incl < 32) break;
+      pred -= 32;
     }
     if (timed_out && lane == 0) record_error(p.err, MOE_ERR_DEVICE_TIMEOUT);
 #pragma unroll
@@ -144,7 +165,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
       const int ex = lane + 32 * s;
       if (ex < E) {
         s_excl[ex] = ex_acc[s];
-        if (b > 0) __stcg(&incl[ex], ex_acc[s] + s_cnt[ex]);
+        if (b > 0) __stcg(&incl[ex], ex_acc[s] + s_tot[ex]);
       }
     }
     __threadfence();
@@ -177,7 +198,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
     for (int ex = tid; ex < kMaxExperts; ex += NT) {
       int c = 0;
       if (ex < E) {
-        const int load = s_excl[ex] + s_cnt[ex];
+        const int load = s_excl[ex] + s_tot[ex];
         c = load < p.C ? load : p.C;
         drop += static_cast<unsigned long long>(load - c);
         p.counts[ex] = c;
@@ -262,7 +283,17 @@ cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st) {
   // the ticket and the block status words start at zero on every call
   cudaError_t e = cudaMemsetAsync(p.ctrl, 0, sizeof(int) * (1 + p.nblk), st);
   if (e != cudaSuccess) return e;
-  dispatch_kernel<<<p.nblk, NT, 0, st>>>(p);
+  const long long Tk = static_cast<long long>(p.T) * p.k;
+  if (dispatch_items(Tk) == kDispatchItemsSmall) {
+    const size_t smem = sizeof(int) * kDispatchItemsSmall * NWARP * p.E;
+    dispatch_kernel<kDispatchItemsSmall><<<p.nblk, NT, smem, st>>>(p);
+  } else {
+    const size_t smem = sizeof(int) * kDispatchItemsLarge * NWARP * p.E;
+    e = cudaFuncSetAttribute(dispatch_kernel<kDispatchItemsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    dispatch_kernel<kDispatchItemsLarge><<<p.nblk, NT, smem, st>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -33,7 +33,7 @@ namespace moe {
 namespace {
 
 constexpr int kNoAllocMaxTiles = 256;
-constexpr long long kNoAllocMaxAssignments = static_cast<long long>(kNoAllocMaxTiles) * kDispatchTile;
+constexpr long long kNoAllocMaxAssignments = static_cast<long long>(kNoAllocMaxTiles) * kDispatchItemsLarge * kDispatchThreads;
 // layout in ints: [0] ticket, [1, 1+kNoAllocMaxTiles) tile status,
 // then per-tile expert histograms [tiles][E], then inclusive prefixes [tiles][E]
 constexpr size_t kCtrlInts = 1 + kNoAllocMaxTiles;
@@ -107,7 +107,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C
   dp.ctrl = scratch;  // launch_dispatch clears the ticket and the status flags
   dp.agg = scratch + kAggOffset;
   dp.incl = scratch + kInclOffset;
-  dp.nblk = static_cast<int>(Tk == 0 ? 1 : (Tk + kDispatchTile - 1) / kDispatchTile);
+  dp.nblk = dispatch_nblk(Tk);  // <= kNoAllocMaxTiles for Tk <= kNoAllocMaxAssignments
   dp.stall_block = -1;
   dp.err = error_out;
   if (launch_dispatch(dp, st) != cudaSuccess) return MOE_ERR_CUDA;

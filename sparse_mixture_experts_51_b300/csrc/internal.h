@@ -31,9 +31,19 @@ struct WsLayout {
   int64_t rows;              // R = min(T*k, E*C)
 };
 
-constexpr int kDispatchItemsPerThread = 16;
+// Dispatch tiles: 256 threads x `items` consecutive priority positions each.
+// Short batches use 1024-assignment tiles (more CTAs, shorter per-tile
+// work); batches above 262144 assignments use 4096-assignment tiles.  Either
+// way at most 256 tiles cover up to 2^20 assignments.
 constexpr int kDispatchThreads = 256;
-constexpr int kDispatchTile = kDispatchItemsPerThread * kDispatchThreads;
+constexpr int kDispatchItemsSmall = 4;
+constexpr int kDispatchItemsLarge = 16;
+constexpr long long kDispatchSmallMax = 256LL * kDispatchItemsSmall * kDispatchThreads;
+inline int dispatch_items(long long Tk) { return Tk <= kDispatchSmallMax ? kDispatchItemsSmall : kDispatchItemsLarge; }
+inline int dispatch_nblk(long long Tk) {
+  const long long tile = static_cast<long long>(dispatch_items(Tk)) * kDispatchThreads;
+  return static_cast<int>(Tk == 0 ? 1 : (Tk + tile - 1) / tile);
+}
 
 WsLayout ws_layout(const moe_shape_t& s, int32_t C);
 
@@ -51,6 +61,8 @@ struct RouterParams {
   int* err;
 };
 cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st);
+// the cluster-tiled router kernel (router_tiled.cu), for wide logit tables
+cudaError_t launch_router_tiled(const RouterParams& p, int dtype, cudaStream_t st, int sms);
 
 struct DispatchParams {
   const int32_t* idx;

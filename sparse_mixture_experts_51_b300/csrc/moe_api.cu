@@ -24,7 +24,7 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   const long long Tk = s.T * s.k;
   const long long EC = static_cast<long long>(s.E) * C;
   L.rows = Tk < EC ? Tk : EC;
-  L.nblk_dispatch = static_cast<int>(Tk == 0 ? 1 : (Tk + kDispatchTile - 1) / kDispatchTile);
+  L.nblk_dispatch = dispatch_nblk(Tk);
   const size_t b = dtype_bytes(s.dtype);
   size_t o = 0;
   auto take = [&](size_t bytes) {

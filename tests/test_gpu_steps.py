@@ -137,3 +137,49 @@ def test_dispatch_bounded_wait_reports_timeout():
     ref = O.dispatch(idx.cpu().numpy(), E, C)
     np.testing.assert_array_equal(d2["pos"].cpu().numpy(), ref["pos"])
     assert api.get_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("T,k,E,C", [(20000, 2, 16, 2600), (150000, 2, 8, 40000), (700, 3, 5, 300)],
+                         ids=["40_small_tiles", "large_tiles", "one_tile_E5"])
+def test_dispatch_many_tiles(T, k, E, C):
+    """Dispatch across more tiles than the 32-tile look-back window (1024- and
+    4096-assignment tiles): slots, counts, offsets and drops bit-exact."""
+    g = torch.Generator().manual_seed(T)
+    logits = torch.randn(T, E, generator=g) + torch.linspace(1.0, -1.0, E)
+    idx = logits.topk(k, dim=1).indices.int()
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    d = api.dispatch(idx.cuda(), x.cuda(), E, C)
+    ref = O.dispatch(idx.numpy(), E, C)
+    np.testing.assert_array_equal(d["pos"].cpu().numpy(), ref["pos"])
+    np.testing.assert_array_equal(d["counts"].cpu().numpy(), ref["counts"])
+    np.testing.assert_array_equal(d["offsets"].cpu().numpy(), ref["offsets"])
+    assert int(d["dropped"].item()) == ref["dropped"]
+    assert api.get_device_error(d["ws"]) == 0
+
+
+def test_dispatch_out_of_range_expert_is_reported():
+    """An expert id outside [0, E) takes no slot and sets MOE_ERR_BOUNDS; the
+    other assignments are dispatched as if it were absent."""
+    T, k, E, C = 300, 2, 6, 200
+    g = torch.Generator().manual_seed(9)
+    idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
+    idx[17, 1] = E      # one past the last expert
+    idx[250, 0] = -3    # negative
+    x = torch.randn(T, 64, generator=g).to(torch.bfloat16)
+    d = api.dispatch(idx.cuda(), x.cuda(), E, C)
+    assert api.get_device_error(d["ws"]) == 6  # MOE_ERR_BOUNDS
+    pos = d["pos"].cpu().numpy()
+    assert pos[17, 1] == -1 and pos[250, 0] == -1
+    clean = idx.numpy().copy()
+    clean[17, 1] = -1
+    clean[250, 0] = -1
+    # the oracle on the table without the two bad assignments gives the same slots
+    load = np.zeros(E, dtype=np.int64)
+    for r in range(k):
+        for t in range(T):
+            e = clean[t, r]
+            if e < 0:
+                continue
+            assert pos[t, r] == (load[e] if load[e] < C else -1)
+            load[e] += 1
+    np.testing.assert_array_equal(d["counts"].cpu().numpy(), np.minimum(load, C))
