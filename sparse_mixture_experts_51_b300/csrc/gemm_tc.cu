@@ -8,15 +8,16 @@
 // (the expert FFN of "Mixture-of-Experts Sparse Model Scaling", Core
 // Concepts: each expert is the dense FFN it replaces).
 //
-// Kernel design (one persistent CTA per SM, 256 threads):
+// Kernel design (one persistent CTA per SM, 384 threads):
 //   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
 //               swizzle, 4-stage mbarrier ring (48 KB per stage)
 //   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16,
 //               fp32 accumulator in TMEM; tcgen05.commit frees smem stages
 //   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators,
 //               so the epilogue of one tile overlaps the mainloop of the next)
-//   warps 4-7   epilogue: tcgen05.ld 32 columns at a time, fused activation,
-//               bias, conversion, row-masked 16-byte stores
+//   warps 4-11  epilogue: two warps per TMEM lane quarter, each taking every
+//               other 32-column chunk: tcgen05.ld, fused activation, bias,
+//               conversion, row-masked 16-byte stores
 // SwiGLU puts 128 rows of W1 and the matching 128 rows of W3 into one
 // 256-row B tile, so one accumulator holds gate | up and the epilogue emits
 // 128 columns of h.  Tiles are ordered expert-major, then N, then M, so CTAs
@@ -39,7 +40,8 @@ constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
-constexpr int NTHREADS = 256;
+constexpr int NTHREADS = 384;
+constexpr int EPI_WARPS = 8;  // warps 4-11: two per TMEM lane quarter, each half of the columns
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers etc*/ +
                            2 * (kMaxExperts + 1) * 4;
 
@@ -59,7 +61,10 @@ struct GemmArgs {
 };
 
 __device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
-__device__ __forceinline__ float silu_f(float a) { return a / (1.0f + expf(-a)); }
+// silu(a) = a / (1 + e^-a) with the fast exponential and division intrinsics:
+// the result is rounded to bf16, far coarser than their error; the exponent
+// is clamped so the divisor stays finite.
+__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(fminf(-a, 80.0f))); }
 
 struct TileInfo {
   int e, row0, rows_valid, n0;
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 4);
+      mbar_init(smem_u32(&tempty[a]), EPI_WARPS);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -222,7 +227,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= 4) {
     // ================= epilogue =================
-    const int q = warp - 4;                 // TMEM lane quarter
+    const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 4) >> 2;       // which half of the 32-column chunks
     const int rloc = q * 32 + lane;         // row inside the tile
     int acc = 0;
     uint32_t aphase = 0;
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if constexpr (MODE == MODE_SWIGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
-        for (int c = 0; c < BN_OUT / 32; ++c) {
+        for (int c = half; c < BN_OUT / 32; c += 2) {
           float gv[32], uv[32];
           tmem_ld32(tbase + c * 32, gv);
           tmem_ld32(tbase + 128 + c * 32, uv);
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else if constexpr (MODE == MODE_GELU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
-        for (int c = 0; c < BN_OUT / 32; ++c) {
+        for (int c = half; c < BN_OUT / 32; c += 2) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
@@ -279,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else {
         float* out = static_cast<float*>(g.out);
 #pragma unroll 1
-        for (int c = 0; c < BN_OUT / 32; ++c) {
+        for (int c = half; c < BN_OUT / 32; c += 2) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
