@@ -9,12 +9,12 @@
 // Concepts: each expert is the dense FFN it replaces).
 //
 // Kernel design (one persistent CTA per SM, 384 threads):
-//   warp 0      TMA producer: 128x64 A tile + 256x64 B tile per stage, 128-byte
-//               swizzle, 4-stage mbarrier ring (48 KB per stage)
-//   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16,
-//               fp32 accumulator in TMEM; tcgen05.commit frees smem stages
-//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators,
-//               so the epilogue of one tile overlaps the mainloop of the next)
+//   warp 0      TMA producer: 128x64 (or 256x64) A tile + 256x64 B tile per
+//               stage, 128-byte swizzle, mbarrier ring of 4 x 48 KB (3 x 64 KB)
+//   warp 1      MMA issuer: one thread issues tcgen05.mma M=128 N=256 K=16
+//               (per M tile), fp32 accumulator in TMEM; tcgen05.commit frees
+//               smem stages
+//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
 //   warps 4-11  epilogue: two warps per TMEM lane quarter, each taking every
 //               other 32-column chunk: tcgen05.ld, fused activation, bias,
 //               conversion, row-masked 16-byte stores
@@ -35,15 +35,28 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NTHREADS = 384;
-constexpr int EPI_WARPS = 8;  // warps 4-11: two per TMEM lane quarter, each half of the columns
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers etc*/ +
-                           2 * (kMaxExperts + 1) * 4;
+constexpr int EPI_WARPS = 8;  // warps 4-11, two per TMEM lane quarter
+
+// MT = M tiles of 128 rows per CTA tile.  MT = 1: 128x256 tiles, 4 stages of
+// 48 KB, two TMEM accumulators (the epilogue of one tile overlaps the next
+// tile's mainloop).  MT = 2: 256x256 tiles that share each B stage between
+// two M tiles (a third less L2->SM traffic per flop), 3 stages of 64 KB, one
+// accumulator pair filling TMEM (the epilogue is not overlapped).
+template <int MT>
+struct Cfg {
+  static constexpr int STAGES = MT == 1 ? 4 : 3;
+  static constexpr int A_BYTES = MT * BM * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator buffers
+  static constexpr int ACC_COLS = 256 * MT;     // TMEM columns per buffer
+  static constexpr int TILE_M = BM * MT;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers etc*/ +
+                                    2 * (kMaxExperts + 1) * 4;
+};
 
 enum { MODE_GELU = 0, MODE_SWIGLU = 1, MODE_DOWN = 2 };
 
@@ -70,10 +83,12 @@ struct TileInfo {
   int e, row0, rows_valid, n0;
 };
 
-template <int MODE>
+template <int MODE, int MT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmB3, GemmArgs g) {
+  using C = Cfg<MT>;
+  constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES, NACC = C::NACC;
   constexpr int BN_OUT = MODE == MODE_SWIGLU ? 128 : 256;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte align the tile ring (128-byte swizzle atoms)
@@ -97,7 +112,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // ---- per-expert tile counts from the segment offsets
   for (int e = tid; e < E; e += NTHREADS) {
     const int cnt = g.offsets[e + 1] - g.offsets[e];
-    s_mt[e] = cnt > 0 ? (cnt + BM - 1) / BM : 0;
+    s_mt[e] = cnt > 0 ? (cnt + C::TILE_M - 1) / C::TILE_M : 0;
   }
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -146,8 +161,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int seg0 = g.offsets[ecur];
     const int cnt = g.offsets[ecur + 1] - seg0;
     ti.e = ecur;
-    ti.row0 = seg0 + mb * BM;
-    ti.rows_valid = min(BM, cnt - mb * BM);
+    ti.row0 = seg0 + mb * C::TILE_M;
+    ti.rows_valid = min(C::TILE_M, cnt - mb * C::TILE_M);
     ti.n0 = nb * BN_OUT;
   };
 
@@ -198,18 +213,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aphase ^ 1u, g.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, g.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          const uint64_t da = smem_desc_sw128(sa), db = smem_desc_sw128(sb);
+          const uint64_t db = smem_desc_sw128(sb);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            // step 16 bf16 = 32 bytes along K inside the swizzled 128-byte rows
-            umma_bf16(dt, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), IDESC,
-                      (kb | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              // M tile m: rows 128m.. of the A stage (16 KB apart) into TMEM columns 256m..;
+              // step 16 bf16 = 32 bytes along K inside the swizzled 128-byte rows
+              const uint64_t da = smem_desc_sw128(sa + static_cast<uint32_t>(m * BM * BK * 2));
+              umma_bf16(dt + static_cast<uint32_t>(m * 256), da + static_cast<uint64_t>(kk * 2),
+                        db + static_cast<uint64_t>(kk * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(smem_u32(&empty[stage]));
           any = true;
@@ -217,7 +237,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok) break;
         umma_commit(smem_u32(&tfull[acc]));
-        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+        if (++acc == NACC) { acc = 0; aphase ^= 1u; }
       }
       if (any) {
         // every MMA issued by this thread has finished before TMEM is freed
@@ -227,9 +247,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= 4) {
     // ================= epilogue =================
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 4) >> 2;       // which half of the 32-column chunks
-    const int rloc = q * 32 + lane;         // row inside the tile
+    // MT = 1: warps w and w+4 share lane quarter w & 3, taking alternate
+    // 32-column chunks; MT = 2: warps 4-7 drain M tile 0, warps 8-11 M tile 1
+    const int q = warp & 3;                             // TMEM lane quarter this warp may access
+    const int msel = MT == 2 ? (warp - 4) >> 2 : 0;     // M tile of the CTA tile
+    const int cfirst = MT == 2 ? 0 : (warp - 4) >> 2;   // first 32-column chunk
+    constexpr int CSTEP = MT == 2 ? 1 : 2;
+    const int rloc = msel * BM + q * 32 + lane;         // row inside the tile
     int acc = 0;
     uint32_t aphase = 0;
     int ecur = 0;
@@ -238,13 +262,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       decode(tile, ecur, ti);
       if (!mbar_wait_bounded(smem_u32(&tfull[acc]), aphase, g.err, abort_flag)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * C::ACC_COLS + msel * 256);
       const bool row_ok = rloc < ti.rows_valid;
       const long long row = static_cast<long long>(ti.row0) + rloc;
       if constexpr (MODE == MODE_SWIGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
-        for (int c = half; c < BN_OUT / 32; c += 2) {
+        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
           float gv[32], uv[32];
           tmem_ld32(tbase + c * 32, gv);
           tmem_ld32(tbase + 128 + c * 32, uv);
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else if constexpr (MODE == MODE_GELU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
-        for (int c = half; c < BN_OUT / 32; c += 2) {
+        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
@@ -285,7 +310,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       } else {
         float* out = static_cast<float*>(g.out);
 #pragma unroll 1
-        for (int c = half; c < BN_OUT / 32; c += 2) {
+        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
@@ -304,7 +329,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-      if (++acc == 2) { acc = 0; aphase ^= 1u; }
+      if (++acc == NACC) { acc = 0; aphase ^= 1u; }
     }
   }
 
@@ -345,17 +370,18 @@ cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, int K, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, int MT>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const GemmArgs& g,
                         long long rows_bound, int num_sms, cudaStream_t st) {
-  auto kern = grouped_gemm_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  auto kern = grouped_gemm_kernel<MODE, MT>;
+  constexpr int smem = Cfg<MT>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // upper bound on tiles: every expert may add one partial M tile
-  const long long mt_bound = (rows_bound + BM - 1) / BM + g.E;
+  const long long mt_bound = (rows_bound + Cfg<MT>::TILE_M - 1) / Cfg<MT>::TILE_M + g.E;
   const long long tiles_bound = mt_bound * g.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(num_sms, std::max<long long>(1, tiles_bound)));
-  kern<<<grid, NTHREADS, SMEM_BYTES, st>>>(a, b, b3, g);
+  kern<<<grid, NTHREADS, smem, st>>>(a, b, b3, g);
   return cudaGetLastError();
 }
 
@@ -370,15 +396,19 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
 
   const bool swiglu = p.act == MOE_ACT_SWIGLU;
+  // 256-row tiles when experts are expected to hold more than four M tiles
+  // (the unoverlapped epilogue then costs little and the shared B stage
+  // pays); 128-row tiles otherwise
+  const int MT = p.rows > 4LL * BM * p.E ? 2 : 1;
   CUtensorMap mA1, mB1, mB3, mA2, mB2;
-  if ((e = make_map(&mA1, p.x_perm, p.rows, p.d, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mA1, p.x_perm, p.rows, p.d, BM * MT)) != cudaSuccess) return e;
   if ((e = make_map(&mB1, p.W1, static_cast<long long>(p.E) * p.F, p.d, swiglu ? BN / 2 : BN)) != cudaSuccess) return e;
   if (swiglu) {
     if ((e = make_map(&mB3, p.W3, static_cast<long long>(p.E) * p.F, p.d, BN / 2)) != cudaSuccess) return e;
   } else {
     mB3 = mB1;
   }
-  if ((e = make_map(&mA2, p.h, p.rows, p.F, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mA2, p.h, p.rows, p.F, BM * MT)) != cudaSuccess) return e;
   if ((e = make_map(&mB2, p.W2, static_cast<long long>(p.E) * p.d, p.F, BN)) != cudaSuccess) return e;
 
   GemmArgs g1{};
@@ -392,8 +422,12 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   g1.out_ld = p.F;
   g1.bias = swiglu ? nullptr : p.b1;
   g1.err = p.err;
-  e = swiglu ? launch_mode<MODE_SWIGLU>(mA1, mB1, mB3, g1, p.rows, sms, st)
-             : launch_mode<MODE_GELU>(mA1, mB1, mB3, g1, p.rows, sms, st);
+  if (MT == 2)
+    e = swiglu ? launch_mode<MODE_SWIGLU, 2>(mA1, mB1, mB3, g1, p.rows, sms, st)
+               : launch_mode<MODE_GELU, 2>(mA1, mB1, mB3, g1, p.rows, sms, st);
+  else
+    e = swiglu ? launch_mode<MODE_SWIGLU, 1>(mA1, mB1, mB3, g1, p.rows, sms, st)
+               : launch_mode<MODE_GELU, 1>(mA1, mB1, mB3, g1, p.rows, sms, st);
   if (e != cudaSuccess) return e;
   if (between_gemms != nullptr && (e = cudaEventRecord(between_gemms, st)) != cudaSuccess) return e;
 
@@ -408,7 +442,8 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   g2.out_ld = p.d;
   g2.bias = p.b2;
   g2.err = p.err;
-  return launch_mode<MODE_DOWN>(mA2, mB2, mB2, g2, p.rows, sms, st);
+  return MT == 2 ? launch_mode<MODE_DOWN, 2>(mA2, mB2, mB2, g2, p.rows, sms, st)
+                 : launch_mode<MODE_DOWN, 1>(mA2, mB2, mB2, g2, p.rows, sms, st);
 }
 
 }  // namespace moe

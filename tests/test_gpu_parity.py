@@ -47,6 +47,10 @@ SMALL = [
     # more than one dispatch tile (T*k > 4096) with drops
     W.Workload("multi_tile_dispatch", T=2500, d=128, E=8, k=2, F=128, act=W.ACT_SWIGLU, capacity_factor=0.9,
                dtype=torch.bfloat16, seed=15),
+    # GELU with 256-row CTA tiles (more than four M tiles per expert), a ragged
+    # last M tile and an N tile wider than F
+    W.Workload("gelu_wide_m_tiles", T=3000, d=256, E=4, k=2, F=320, act=W.ACT_GELU, capacity_factor=1.0,
+               dtype=torch.bfloat16, seed=17),
     # fp32 layer with nonzero-bias experts and noise
     W.Workload("fp32_noisy", T=150, d=48, E=5, k=2, F=40, act=W.ACT_GELU, capacity_factor=1.0,
                dtype=torch.float32, seed=16, noisy=True, zipf_bias=True, expert_bias=True),
