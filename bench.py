@@ -52,6 +52,7 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="launch every kernel from the host (no CUDA graph)")
     return ap.parse_args(argv)
 
 
@@ -131,6 +132,17 @@ class ClockSampler:
                 pass
             time.sleep(self.period)
 
+    def wait_started(self, timeout_s: float = 3.0):
+        """Returns once the first clock sample is in (or after timeout_s)."""
+        t0 = time.time()
+        if self.mode == "nvml":
+            while not self.samples and time.time() - t0 < timeout_s:
+                time.sleep(0.005)
+        elif self.mode == "nvidia-smi":
+            # nvidia-smi prints its first sample right after it starts
+            while time.time() - t0 < min(timeout_s, 1.0):
+                time.sleep(0.05)
+
     def __enter__(self):
         if self.mode == "nvml":
             self.t = threading.Thread(target=self._run_nvml, daemon=True)
@@ -138,7 +150,7 @@ class ClockSampler:
         elif self.mode == "nvidia-smi":
             import subprocess
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
@@ -294,16 +306,23 @@ def run_ours(a):
     counts = torch.empty(w.E, dtype=torch.int32, device=dev)
     dropped = torch.empty(1, dtype=torch.int64, device=dev)
     stream = torch.cuda.current_stream(dev)
-    sptr = ctypes.c_void_p(stream.cuda_stream)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     P = api._ptr
 
     def fwd_args():
+        # the stream current at the call (the capture stream while a graph is recorded)
+        sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
         return [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
                 P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), P(out),
                 None, None, None, None, P(counts), None, P(dropped), None, P(ws), ws.numel(), sptr]
 
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(a.steps)]
+    # the timed steps run as CUDA graphs of up to GRAPH_STEPS steps each (every
+    # step the same C-ABI call, moe_forward_timed, its launches replayed
+    # without host gaps); the L2 flush between steps lies outside each
+    # step's events, and the events of a graph are read after each replay
+    GRAPH_STEPS = 250
+    G = min(a.steps, GRAPH_STEPS)
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(G)]
 
     def step_timed(i):
         arr = (ctypes.c_void_p * 6)(*[ctypes.c_void_p(e.cuda_event) for e in stage_ev[i]])
@@ -321,15 +340,42 @@ def run_ours(a):
     torch.cuda.synchronize()
     assert api.get_device_error(ws) == 0
 
+    graphs = {}
+
+    def graph_of(n):
+        if n not in graphs:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                for i in range(n):
+                    flush.zero_()
+                    step_timed(i)
+            torch.cuda.synchronize()
+            graphs[n] = gr
+        return graphs[n]
+
+    chunks = [G] * (a.steps // G) + ([a.steps % G] if a.steps % G else [])
+    if not a.eager:
+        for n in set(chunks):
+            graph_of(n)
+
+    step_ms, stage_ms = [], [[] for _ in range(5)]
     sampler = ClockSampler(local)
     with sampler:
+        sampler.wait_started()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        for i in range(a.steps):
-            flush.zero_()
-            step_timed(i)
-        torch.cuda.synchronize()
+        for n in chunks:
+            if a.eager:
+                for i in range(n):
+                    flush.zero_()
+                    step_timed(i)
+            else:
+                graphs[n].replay()
+            torch.cuda.synchronize()
+            step_ms += [evs[0].elapsed_time(evs[5]) for evs in stage_ev[:n]]
+            for j in range(5):
+                stage_ms[j] += [evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev[:n]]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
@@ -337,8 +383,6 @@ def run_ours(a):
     if err != 0:
         raise RuntimeError(f"device-side error {err} during the timed region")
 
-    step_ms = [evs[0].elapsed_time(evs[5]) for evs in stage_ev]
-    stage_ms = [[evs[j].elapsed_time(evs[j + 1]) for evs in stage_ev] for j in range(5)]
     total_ms = sum(step_ms)
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
@@ -424,7 +468,8 @@ def run_ours(a):
 
     cfg = workload_config(w)
     cfg.update({"C": C, "kept_rows": int(sum(cnt)), "dropped": int(dropped.item()),
-                "parallelism": "replicas" if world > 1 else "single_gpu"})
+                "parallelism": "replicas" if world > 1 else "single_gpu",
+                "launch": "eager" if a.eager else f"CUDA graphs of up to {GRAPH_STEPS} timed steps (moe_forward_timed each)"})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic", "config": cfg,

@@ -167,6 +167,19 @@ class MoELayer:
         self._ws = {}
         self.last = None
 
+    def capture(self, x: torch.Tensor, eps: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None) -> "CapturedForward":
+        """Capture this layer's forward over the device buffers x (and eps)
+        into a CUDA graph.  The routing outputs of replays are not kept."""
+        if out is None:
+            out = torch.empty(x.shape[0], self.d, dtype=x.dtype, device=x.device)
+        keep = self.keep_routing
+        self.keep_routing = False
+        try:
+            return _capture(self, x, eps, out)
+        finally:
+            self.keep_routing = keep
+
     def capacity(self, T: int) -> int:
         return self.C_fixed if self.C_fixed is not None else capacity(T, self.k, self.E, self.capacity_factor)
 
@@ -210,6 +223,33 @@ class MoELayer:
         return out
 
 
+class CapturedForward:
+    """A CUDA graph of one MoELayer forward over fixed device buffers.
+
+    ``replay()`` re-runs the captured forward on whatever the static input
+    buffers (``x``, ``eps``) hold at that moment and writes ``out``; all
+    launches of the layer go to the GPU as one graph launch.  Build it with
+    ``MoELayer.capture``."""
+
+    def __init__(self, graph, x, eps, out):
+        self.graph, self.x, self.eps, self.out = graph, x, eps, out
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
+
+
+def _capture(layer, x, eps, out):
+    # one eager call first: per-device set-up (attribute queries, launch
+    # limits) happens outside the capture
+    layer(x, eps=eps, out=out)
+    torch.cuda.synchronize(x.device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer(x, eps=eps, out=out)
+    return CapturedForward(graph, x, eps, out)
+
+
 def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=None, b1=None, b2=None,
             capacity_factor: Optional[float] = None, C: Optional[int] = None, want_moe: bool = False,
             stats: Optional[torch.Tensor] = None, stream=None):
@@ -225,4 +265,4 @@ def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=No
 
 
 __all__ = ["capacity", "max_rows", "workspace_size", "new_workspace", "get_device_error", "route", "dispatch",
-           "expert_ffn", "combine", "forward", "MoELayer", "MoeError", "shape_of"]
+           "expert_ffn", "combine", "forward", "MoELayer", "CapturedForward", "MoeError", "shape_of"]

@@ -429,7 +429,13 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
     e = swiglu ? launch_mode<MODE_SWIGLU, 1>(mA1, mB1, mB3, g1, p.rows, sms, st)
                : launch_mode<MODE_GELU, 1>(mA1, mB1, mB3, g1, p.rows, sms, st);
   if (e != cudaSuccess) return e;
-  if (between_gemms != nullptr && (e = cudaEventRecord(between_gemms, st)) != cudaSuccess) return e;
+  if (between_gemms != nullptr) {
+    // an external record node when captured into a graph, so it still times
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(st, &cs)) != cudaSuccess) return e;
+    const unsigned int flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    if ((e = cudaEventRecordWithFlags(between_gemms, st, flags)) != cudaSuccess) return e;
+  }
 
   GemmArgs g2{};
   g2.offsets = p.offsets;

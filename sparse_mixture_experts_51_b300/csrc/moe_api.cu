@@ -314,9 +314,17 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
 
   const WsLayout L = ws_layout(*shape, C);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Inside a stream capture the stage events become external event-record
+  // nodes, which record (and time) on every graph launch.
+  unsigned int rec_flags = cudaEventRecordDefault;
+  if (stage_events != nullptr) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
+  }
   auto mark = [&](int i) -> moe_status_t {
     if (stage_events == nullptr) return MOE_OK;
-    return cuda_status(cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), s));
+    return cuda_status(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, rec_flags));
   };
   if (idx == nullptr) idx = at<int32_t>(ws, L.idx);
   if (w == nullptr) w = at<float>(ws, L.w);

@@ -167,3 +167,23 @@ def test_determinism():
     b = gpu_forward(w, g)
     for key in ("out", "moe", "idx", "w", "pos", "counts", "offsets", "dropped"):
         assert torch.equal(a[key], b[key]), key
+
+
+def test_cuda_graph_replay_matches_eager():
+    """MoELayer.capture: a CUDA-graph replay of the forward gives the eager
+    output bit for bit, also after new tokens are copied into the input."""
+    w = SMALL[0]
+    inp = W.make_inputs(w)
+    g = to_gpu(inp)
+    layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, "swiglu", W3=g["W3"], capacity_factor=w.capacity_factor,
+                         keep_routing=False)
+    x = g["x"].clone()
+    cap = layer.capture(x)
+    eager = layer(x)
+    torch.cuda.synchronize()
+    assert torch.equal(cap.replay(), eager)
+    x2 = torch.randn(x.shape, generator=torch.Generator().manual_seed(77)).to(x.dtype).cuda()
+    x.copy_(x2)
+    out2 = cap.replay().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, layer(x2))
