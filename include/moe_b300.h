@@ -220,13 +220,18 @@ MOE_API moe_status_t moe_forward(const moe_shape_t* shape, double capacity_facto
                          int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
                          void* ws, size_t ws_bytes, void* stream);
 
-/* moe_forward, recording six CUDA events (cudaEvent_t, created by the
+/* moe_forward, recording up to six CUDA events (cudaEvent_t, created by the
  * caller) on `stream` at the stage boundaries, so each stage can be timed
  * with cudaEventElapsedTime:
  *   stage_events[0] before the router        [1] after the router
  *   [2] after dispatch + gather              [3] after the first expert GEMM
  *   [4] after the second expert GEMM         [5] after the combine
- * MOE_ERR_INVALID_ARG if stage_events or any of its six entries is NULL. */
+ * A NULL entry records nothing at that boundary.  The layer's kernels are
+ * launched with programmatic dependent launch, so a kernel may start its
+ * prologue while its predecessor finishes; an event between two kernels
+ * orders them fully.  While `stream` is being captured into a CUDA graph the
+ * events are recorded as external event nodes (they time every launch of
+ * the graph).  MOE_ERR_INVALID_ARG if stage_events is NULL. */
 MOE_API moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
                                        const void* x, const float* W_g, const float* b_g,
                                        const float* W_noise, const float* eps, const void* W1,

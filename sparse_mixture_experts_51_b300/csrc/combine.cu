@@ -39,69 +39,93 @@ __device__ __forceinline__ void store4<float>(float* p, const float (&v)[4]) {
 }
 template <>
 __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const float (&v)[4]) {
-  __nv_bfloat162 h[2] = {__floats2bfloat162_rn(v[0], v[1]), __floats2bfloat162_rn(v[2], v[3])};
-  *reinterpret_cast<uint2*>(p) = *reinterpret_cast<const uint2*>(h);
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v[0], v[1]), b = __floats2bfloat162_rn(v[2], v[3]);
+  uint2 u;
+  u.x = *reinterpret_cast<const uint32_t*>(&a);
+  u.y = *reinterpret_cast<const uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
 }
 
-// One thread per (token, 8-element chunk): it resolves the token's kept
-// expert rows (k small loads, L1-resident across the token's chunks), issues
-// every 16-byte load of the chunk at once (k expert rows, the residual), and
-// writes the chunk once.  Ranks are summed in order 0..k-1 in fp32.
-template <typename TO>
+// One thread per (token, V-element chunk), V = 8 or 16: it resolves the
+// token's kept expert rows (from the grouped-row map when the dispatch wrote
+// one, else from idx / pos / offsets), issues every 16-byte load of the
+// chunk at once (k expert rows, the residual), and writes the chunk once.
+// Ranks are summed in order 0..k-1 in fp32.
+template <typename TO, int V>
 __global__ void __launch_bounds__(256) combine_kernel(CombineParams p, long long items, int chunks) {
+  pdl_wait();
+  pdl_trigger();
   const long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (it >= items) return;
   const long long t = it / chunks;
-  const int c = static_cast<int>(it - t * chunks) * 8;
+  const int c = static_cast<int>(it - t * chunks) * V;
   const int k = p.k, d = p.d;
   // the residual chunk first: its load overlaps the expert-row loads
   const TO* res = static_cast<const TO*>(p.residual);
-  float r0[4] = {0.f, 0.f, 0.f, 0.f}, r1[4] = {0.f, 0.f, 0.f, 0.f};
+  float rv[V];
   if (res) {
-    load4<TO>(res + t * d + c, r0);
-    load4<TO>(res + t * d + c + 4, r1);
-  }
-  float acc[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int q = 0; q < V; q += 4) {
+      float r4[4];
+      load4<TO>(res + t * d + c + q, r4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rv[q + i] = r4[i];
+    }
+  }
+  float acc[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) acc[i] = 0.f;
 #pragma unroll 2
   for (int r = 0; r < k; ++r) {
-    const int ps = __ldg(p.pos + t * k + r);
-    if (ps < 0) continue;
-    const int e = __ldg(p.idx + t * k + r);
     long long row = -1;
-    if (e >= 0 && e < p.E) row = static_cast<long long>(__ldg(p.offsets + e)) + ps;
-    if (row < 0 || row >= p.rows) {
+    if (p.row_of) {
+      row = __ldg(p.row_of + t * k + r);
+    } else {
+      const int ps = __ldg(p.pos + t * k + r);
+      if (ps >= 0) {
+        const int e = __ldg(p.idx + t * k + r);
+        if (e >= 0 && e < p.E) row = static_cast<long long>(__ldg(p.offsets + e)) + ps;
+        if (row < 0) record_error(p.err, MOE_ERR_BOUNDS);
+      }
+    }
+    if (row < 0) continue;  // dropped: the residual carries the token
+    if (row >= p.rows) {
       record_error(p.err, MOE_ERR_BOUNDS);
       continue;
     }
     const float wt = __ldg(p.w + t * k + r);
     const float4* src = reinterpret_cast<const float4*>(p.y_perm + row * d + c);
-    const float4 a = __ldg(src), b = __ldg(src + 1);
-    acc[0] = fmaf(wt, a.x, acc[0]); acc[1] = fmaf(wt, a.y, acc[1]);
-    acc[2] = fmaf(wt, a.z, acc[2]); acc[3] = fmaf(wt, a.w, acc[3]);
-    acc[4] = fmaf(wt, b.x, acc[4]); acc[5] = fmaf(wt, b.y, acc[5]);
-    acc[6] = fmaf(wt, b.z, acc[6]); acc[7] = fmaf(wt, b.w, acc[7]);
+    float4 yv[V / 4];
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) yv[q] = __ldg(src + q);
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      acc[4 * q] = fmaf(wt, yv[q].x, acc[4 * q]);
+      acc[4 * q + 1] = fmaf(wt, yv[q].y, acc[4 * q + 1]);
+      acc[4 * q + 2] = fmaf(wt, yv[q].z, acc[4 * q + 2]);
+      acc[4 * q + 3] = fmaf(wt, yv[q].w, acc[4 * q + 3]);
+    }
   }
   if (p.moe_out) {
     float4* mo = reinterpret_cast<float4*>(p.moe_out + t * d + c);
-    mo[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    mo[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-  }
-  float o0[4], o1[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o0[i] = res ? r0[i] + acc[i] : acc[i];
-    o1[i] = res ? r1[i] + acc[4 + i] : acc[4 + i];
+    for (int q = 0; q < V / 4; ++q) mo[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
   }
   TO* out = static_cast<TO*>(p.out);
-  store4<TO>(out + t * d + c, o0);
-  store4<TO>(out + t * d + c + 4, o1);
+#pragma unroll
+  for (int q = 0; q < V; q += 4) {
+    float o4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o4[i] = res ? rv[q + i] + acc[q + i] : acc[q + i];
+    store4<TO>(out + t * d + c + q, o4);
+  }
 }
 
 // d not a multiple of 8 (fp32 layers with d % 4 == 0): one warp per token, 4 elements per lane.
 template <typename TO>
 __global__ void __launch_bounds__(256) combine_kernel4(CombineParams p) {
+  pdl_wait();
+  pdl_trigger();
   const long long t = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= p.T) return;
@@ -109,11 +133,16 @@ __global__ void __launch_bounds__(256) combine_kernel4(CombineParams p) {
   for (int c = lane * 4; c < d; c += 128) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int r = 0; r < k; ++r) {
-      const int ps = p.pos[t * k + r];
-      if (ps < 0) continue;
-      const int e = p.idx[t * k + r];
       long long row = -1;
-      if (e >= 0 && e < p.E) row = static_cast<long long>(p.offsets[e]) + ps;
+      if (p.row_of) {
+        row = p.row_of[t * k + r];
+        if (row < 0) continue;
+      } else {
+        const int ps = p.pos[t * k + r];
+        if (ps < 0) continue;
+        const int e = p.idx[t * k + r];
+        if (e >= 0 && e < p.E) row = static_cast<long long>(p.offsets[e]) + ps;
+      }
       if (row < 0 || row >= p.rows) {
         record_error(p.err, MOE_ERR_BOUNDS);
         continue;
@@ -147,6 +176,8 @@ __device__ __forceinline__ int expert_of_row(const int32_t* offsets, int E, long
 
 // h[row, f] = act(x_perm[row] . W1[e, f] (+ b1[e, f]))   (SwiGLU: silu(.) * x_perm[row] . W3[e, f])
 __global__ void __launch_bounds__(256) ffn1_f32_kernel(FfnParams p) {
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int f = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -173,6 +204,8 @@ __global__ void __launch_bounds__(256) ffn1_f32_kernel(FfnParams p) {
 
 // y_perm[row, i] = h[row] . W2[e, i] (+ b2[e, i])
 __global__ void __launch_bounds__(256) ffn2_f32_kernel(FfnParams p) {
+  pdl_wait();
+  pdl_trigger();
   const long long row = blockIdx.x;
   const int i = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -192,20 +225,32 @@ __global__ void __launch_bounds__(256) ffn2_f32_kernel(FfnParams p) {
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st) {
   if (p.T == 0) return cudaSuccess;
-  if (p.d % 8 == 0) {
+  if (p.d % 16 == 0) {
+    const int chunks = p.d / 16;
+    const long long items = static_cast<long long>(p.T) * chunks;
+    const long long blocks = (items + 255) / 256;
+    if (p.dtype == MOE_BF16)
+      return launch_pdl(combine_kernel<__nv_bfloat16, 16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p,
+                        items, chunks);
+    else
+      return launch_pdl(combine_kernel<float, 16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, items,
+                        chunks);
+  } else if (p.d % 8 == 0) {
     const int chunks = p.d / 8;
     const long long items = static_cast<long long>(p.T) * chunks;
     const long long blocks = (items + 255) / 256;
     if (p.dtype == MOE_BF16)
-      combine_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, items, chunks);
+      return launch_pdl(combine_kernel<__nv_bfloat16, 8>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p,
+                        items, chunks);
     else
-      combine_kernel<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, items, chunks);
+      return launch_pdl(combine_kernel<float, 8>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, items,
+                        chunks);
   } else {
     const long long blocks = (static_cast<long long>(p.T) * 32 + 255) / 256;
     if (p.dtype == MOE_BF16)
-      combine_kernel4<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+      return launch_pdl(combine_kernel4<__nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p);
     else
-      combine_kernel4<float><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+      return launch_pdl(combine_kernel4<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p);
   }
   return cudaGetLastError();
 }
@@ -213,12 +258,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st) {
 cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st) {
   if (p.rows == 0) return cudaSuccess;
   dim3 g1(static_cast<unsigned>(p.rows), static_cast<unsigned>((p.F + 7) / 8));
-  ffn1_f32_kernel<<<g1, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(ffn1_f32_kernel, g1, dim3(256), 0, st, 1, p);
   if (e != cudaSuccess) return e;
   dim3 g2(static_cast<unsigned>(p.rows), static_cast<unsigned>((p.d + 7) / 8));
-  ffn2_f32_kernel<<<g2, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(ffn2_f32_kernel, g2, dim3(256), 0, st, 1, p);
 }
 
 }  // namespace moe

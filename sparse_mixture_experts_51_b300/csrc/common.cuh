@@ -29,6 +29,17 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- dependent launch
+// Kernels of the layer are launched with programmatic stream serialisation:
+// a kernel may start while its predecessor on the stream is finishing, runs
+// its prologue (nothing that reads the predecessor's outputs), and waits
+// here until the predecessor has completed and its writes are visible.
+// Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream begin its prologue (it still waits for
+// this grid to complete before reading anything this grid writes).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- smem address
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

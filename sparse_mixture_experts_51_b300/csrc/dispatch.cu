@@ -14,7 +14,7 @@
 //     obtains its tile index from a ticket counter, so a block only ever
 //     waits on blocks that are already running;
 //   * all ITEMS expert ids of a thread are loaded at once; warps rank equal
-//     experts with match.any + popc, the per-(step, warp, expert) counts go
+//     experts with per-bit ballots + popc, the per-(step, warp, expert) counts go
 //     to shared memory, and one per-expert exclusive scan over the
 //     (step, warp) sequence orders every assignment of the tile;
 //   * the per-expert tile totals are scanned across tiles with a decoupled
@@ -23,7 +23,10 @@
 //     aggregates up to the nearest inclusive prefix; every wait is bounded
 //     and records MOE_ERR_DEVICE_TIMEOUT;
 //   * the block holding the last tile turns the loads into counts, segment
-//     offsets and the drop count.
+//     offsets and the drop count;
+//   * the last block to finish (a done counter) clears the ticket, the status
+//     flags and the counter, so the next call finds them at zero without a
+//     separate memset (the workspace is zero-filled once, at allocation).
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,6 +35,18 @@ namespace {
 
 constexpr int NT = kDispatchThreads;
 constexpr int NWARP = NT / 32;
+
+// Lanes of the warp holding the same value v in [0, 2^nbits): one ballot per
+// bit, intersected (a constant-cost stand-in for match.any).
+__device__ __forceinline__ unsigned same_value_lanes(int v, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const bool bit = (v >> b) & 1;
+    const unsigned on = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? on : ~on;
+  }
+  return m;
+}
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -54,6 +69,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
   const int E = p.E;
   const long long total = static_cast<long long>(p.T) * p.k;
 
+  pdl_wait();  // the top-k table is the predecessor's output
   if (tid == 0) s_ticket = atomicAdd(&p.ctrl[0], 1);
   for (int i = tid; i < ITEMS * NWARP * E; i += NT) s_hist[i] = 0;
   __syncthreads();
@@ -76,6 +92,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
   }
   // ---- rank inside the warp step; per-(step, warp, expert) counts
   const unsigned lt_mask = (1u << lane) - 1u;
+  const int nbits = 32 - __clz(E);  // expert ids + 1 lie in [0, E] < 2^nbits
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     int e = my_e[i];
@@ -85,7 +102,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
       e = -1;
     }
     my_e[i] = e;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const unsigned peers = same_value_lanes(e + 1, nbits);
     my_rank[i] = __popc(peers & lt_mask);
     if (e >= 0 && my_rank[i] == 0) s_hist[(i * NWARP + warp) * E + e] = __popc(peers);
   }
@@ -238,27 +255,173 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
       }
     }
   }
+
+  // ---- every block is past its look-back: the last one to get here clears
+  // the control words for the next call
+  pdl_trigger();
+  __syncthreads();
+  if (tid == 0) {
+    int* done = p.ctrl + 1 + p.nblk;
+    __threadfence();
+    if (atomicAdd(done, 1) == p.nblk - 1) {
+      for (int i = 0; i < p.nblk; ++i) status[i] = 0;
+      p.ctrl[0] = 0;
+      *done = 0;
+      __threadfence();
+    }
+  }
+}
+
+// Single-CTA dispatch, for batches whose per-(step, warp, expert) histogram
+// fits in shared memory: 1024 threads take ITEMS assignments each (thread
+// tid, step i: priority position i*1024 + tid), rank equal experts within
+// each warp step with per-bit ballots, and one exclusive scan per expert over the
+// (step, warp) sequence -- a warp per expert, ITEMS entries per lane -- gives
+// every assignment its slot.  No inter-block scan, no atomics, no control
+// words; the same results as the tiled kernel.
+constexpr int SNT = 1024;
+constexpr int SNW = SNT / 32;
+
+template <int ITEMS>
+__global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams p) {
+  extern __shared__ int s_hist[];  // [ITEMS * SNW][E]: counts, then exclusive prefixes
+  __shared__ int s_tot[kMaxExperts];
+  __shared__ unsigned long long s_drop[SNW];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = p.E;
+  const int total = p.T * p.k;  // < 2^31 (checked on the host)
+  constexpr int S = ITEMS * SNW;  // (step, warp) entries per expert
+
+  for (int i = tid; i < S * E; i += SNT) s_hist[i] = 0;
+  pdl_wait();  // the top-k table is the predecessor's output
+  // per item: expert + 1 in bits 0-7 (0: none), rank inside the warp step in bits 8-12
+  int my_er[ITEMS];
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int j = i * SNT + tid;
+    int e = -1;
+    if (j < total) {
+      const int r = j / p.T;
+      const int t = j - r * p.T;
+      e = __ldg(p.idx + t * p.k + r);
+      if (e < 0 || e >= E) {  // an expert id out of range takes no slot
+        record_error(p.err, MOE_ERR_BOUNDS);
+        e = -1;
+      }
+    }
+    my_er[i] = e + 1;
+  }
+  __syncthreads();  // the histogram is zero
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int nbits = 32 - __clz(E);  // expert ids + 1 lie in [0, E] < 2^nbits
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int e = my_er[i] - 1;
+    const unsigned peers = same_value_lanes(my_er[i], nbits);
+    const int rk = __popc(peers & lt_mask);
+    my_er[i] |= rk << 8;
+    if (e >= 0 && rk == 0) s_hist[(i * SNW + warp) * E + e] = __popc(peers);
+  }
+  __syncthreads();
+  // ---- per expert: exclusive scan over the (step, warp) sequence (priority order)
+  for (int ex = warp; ex < E; ex += SNW) {
+    int run = 0;
+    for (int q = 0; q < ITEMS; ++q) run += s_hist[(lane * ITEMS + q) * E + ex];
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int off = incl - run;
+    for (int q = 0; q < ITEMS; ++q) {
+      const int c = s_hist[(lane * ITEMS + q) * E + ex];
+      s_hist[(lane * ITEMS + q) * E + ex] = off;
+      off += c;
+    }
+    if (lane == 31) s_tot[ex] = incl;
+  }
+  __syncthreads();
+  // ---- slots; kept iff below capacity
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i) {
+    const int j = i * SNT + tid;
+    if (j < total) {
+      const int r = j / p.T;
+      const int t = j - r * p.T;
+      int ps = -1;
+      const int e = (my_er[i] & 0xff) - 1;
+      if (e >= 0) {
+        const int slot = s_hist[(i * SNW + warp) * E + e] + (my_er[i] >> 8);
+        ps = slot < p.C ? slot : -1;
+      }
+      p.pos[t * p.k + r] = ps;
+    }
+  }
+  // ---- counts, segment offsets, drop count
+  unsigned long long drop = 0;
+  for (int ex = tid; ex < E; ex += SNT) {
+    const int load = s_tot[ex];
+    const int c = load < p.C ? load : p.C;
+    drop += static_cast<unsigned long long>(load - c);
+    p.counts[ex] = c;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) drop += __shfl_xor_sync(0xffffffffu, drop, o);
+  if (lane == 0) s_drop[warp] = drop;
+  __syncthreads();
+  if (warp == 0) {
+    int v[4], run = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int ex = lane * 4 + q;
+      v[q] = ex < E ? min(s_tot[ex], p.C) : 0;
+      run += v[q];
+    }
+    int incl = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    int off = incl - run;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int ex = lane * 4 + q;
+      if (ex < E) p.offsets[ex] = off;
+      off += v[q];
+    }
+    if (lane == 31) p.offsets[E] = incl;
+    if (lane == 0) {
+      unsigned long long dsum = 0;
+      for (int w2 = 0; w2 < SNW; ++w2) dsum += s_drop[w2];
+      *p.dropped = static_cast<long long>(dsum);
+    }
+  }
+  pdl_trigger();
 }
 
 // One warp per assignment (t, r): copy token t into its expert-ordered row.
 template <int VB>
 __global__ void __launch_bounds__(256) gather_kernel(GatherParams p, long long rows_alloc) {
+  pdl_wait();
+  pdl_trigger();
   const long long a = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long total = static_cast<long long>(p.T) * p.k;
   if (a >= total) return;
   const int ps = p.pos[a];
-  if (ps < 0) return;
-  const int e = p.idx[a];
-  if (e < 0 || e >= p.E) {
-    if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
-    return;
+  const int e = ps >= 0 ? p.idx[a] : -1;
+  long long row = -1;
+  if (ps >= 0) {
+    if (e >= 0 && e < p.E) row = static_cast<long long>(p.offsets[e]) + ps;
+    if (row < 0 || row >= rows_alloc) {
+      if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
+      row = -1;
+    }
   }
-  const long long row = static_cast<long long>(p.offsets[e]) + ps;
-  if (row < 0 || row >= rows_alloc) {
-    if (lane == 0) record_error(p.err, MOE_ERR_BOUNDS);
-    return;
-  }
+  if (lane == 0 && p.row_of) p.row_of[a] = static_cast<int32_t>(row);
+  if (row < 0) return;
   const long long t = a / p.k;
   const long long row_bytes = static_cast<long long>(p.d) * p.elem_bytes;
   const char* src = static_cast<const char*>(p.x) + t * row_bytes;
@@ -279,22 +442,45 @@ __global__ void __launch_bounds__(256) gather_kernel(GatherParams p, long long r
 
 }  // namespace
 
-cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st) {
-  // the ticket and the block status words start at zero on every call
-  cudaError_t e = cudaMemsetAsync(p.ctrl, 0, sizeof(int) * (1 + p.nblk), st);
+namespace {
+template <int ITEMS>
+cudaError_t launch_single(const DispatchParams& p, cudaStream_t st) {
+  const size_t smem = sizeof(int) * static_cast<size_t>(ITEMS) * SNW * p.E;
+  cudaError_t e = cudaFuncSetAttribute(dispatch_single_kernel<ITEMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  return launch_pdl(dispatch_single_kernel<ITEMS>, dim3(1), dim3(SNT), smem, st, 1, p);
+}
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st) {
+  cudaError_t e = cudaSuccess;
   const long long Tk = static_cast<long long>(p.T) * p.k;
+  // one CTA for up to 8192 assignments (8 per thread: more would spill) when
+  // its histogram (items per thread x 32 warps x E ints) fits in 96 KB
+  int items = 1;
+  while (static_cast<long long>(items) * SNT < Tk) items <<= 1;
+  // (the testing hook that stalls a tile needs the tiled kernel)
+  if (p.stall_block < 0 && items <= 8 && static_cast<long long>(items) * SNW * p.E * 4 <= 96 * 1024) {
+    switch (items) {
+      case 1: return launch_single<1>(p, st);
+      case 2: return launch_single<2>(p, st);
+      case 4: return launch_single<4>(p, st);
+      default: return launch_single<8>(p, st);
+    }
+  }
+  if (p.clear_ctrl && (e = cudaMemsetAsync(p.ctrl, 0, sizeof(int) * (2 + p.nblk), st)) != cudaSuccess) return e;
   if (dispatch_items(Tk) == kDispatchItemsSmall) {
     const size_t smem = sizeof(int) * kDispatchItemsSmall * NWARP * p.E;
-    dispatch_kernel<kDispatchItemsSmall><<<p.nblk, NT, smem, st>>>(p);
+    e = launch_pdl(dispatch_kernel<kDispatchItemsSmall>, dim3(p.nblk), dim3(NT), smem, st, 1, p);
   } else {
     const size_t smem = sizeof(int) * kDispatchItemsLarge * NWARP * p.E;
     e = cudaFuncSetAttribute(dispatch_kernel<kDispatchItemsLarge>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dispatch_kernel<kDispatchItemsLarge><<<p.nblk, NT, smem, st>>>(p);
+    e = launch_pdl(dispatch_kernel<kDispatchItemsLarge>, dim3(p.nblk), dim3(NT), smem, st, 1, p);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_gather(const GatherParams& p, cudaStream_t st) {
@@ -304,11 +490,8 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t st) {
   const long long row_bytes = static_cast<long long>(p.d) * p.elem_bytes;
   const bool vec16 = row_bytes % 16 == 0 && reinterpret_cast<uintptr_t>(p.x) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(p.x_perm) % 16 == 0;
-  if (vec16)
-    gather_kernel<16><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, p.rows_alloc);
-  else
-    gather_kernel<4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(p, p.rows_alloc);
-  return cudaGetLastError();
+  if (vec16) return launch_pdl(gather_kernel<16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, p.rows_alloc);
+  return launch_pdl(gather_kernel<4>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, p.rows_alloc);
 }
 
 }  // namespace moe

@@ -34,9 +34,9 @@ namespace {
 
 constexpr int kNoAllocMaxTiles = 256;
 constexpr long long kNoAllocMaxAssignments = static_cast<long long>(kNoAllocMaxTiles) * kDispatchItemsLarge * kDispatchThreads;
-// layout in ints: [0] ticket, [1, 1+kNoAllocMaxTiles) tile status,
+// layout in ints: [0] ticket, [1, 1+kNoAllocMaxTiles) tile status, then a done counter,
 // then per-tile expert histograms [tiles][E], then inclusive prefixes [tiles][E]
-constexpr size_t kCtrlInts = 1 + kNoAllocMaxTiles;
+constexpr size_t kCtrlInts = 2 + kNoAllocMaxTiles;
 constexpr size_t kAggOffset = (kCtrlInts + 63) / 64 * 64;
 constexpr size_t kInclOffset = kAggOffset + static_cast<size_t>(kNoAllocMaxTiles) * kMaxExperts;
 constexpr size_t kScratchInts = kInclOffset + static_cast<size_t>(kNoAllocMaxTiles) * kMaxExperts;
@@ -104,7 +104,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C
   dp.counts = counts;
   dp.offsets = offsets;
   dp.dropped = reinterpret_cast<long long*>(dropped);
-  dp.ctrl = scratch;  // launch_dispatch clears the ticket and the status flags
+  dp.ctrl = scratch;
+  dp.clear_ctrl = 1;  // launch_dispatch clears the ticket, the status flags and the done counter
   dp.agg = scratch + kAggOffset;
   dp.incl = scratch + kInclOffset;
   dp.nblk = dispatch_nblk(Tk);  // <= kNoAllocMaxTiles for Tk <= kNoAllocMaxAssignments

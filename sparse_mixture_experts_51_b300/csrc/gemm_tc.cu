@@ -74,10 +74,19 @@ struct GemmArgs {
 };
 
 __device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
-// silu(a) = a / (1 + e^-a) with the fast exponential and division intrinsics:
-// the result is rounded to bf16, far coarser than their error; the exponent
-// is clamped so the divisor stays finite.
-__device__ __forceinline__ float silu_f(float a) { return __fdividef(a, 1.0f + __expf(fminf(-a, 80.0f))); }
+// silu(a) = a * sigmoid(a) = a * (1 + tanh(a/2)) / 2, with the hardware
+// tanh approximation (tanh.approx.f32, relative error about 2^-11): one
+// special-function op per element instead of an exponential and a
+// reciprocal, and the result is rounded to bf16 (2^-8) right after.
+__device__ __forceinline__ float tanh_approx(float v) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float silu_f(float a) {
+  const float h = 0.5f * a;
+  return fmaf(h, tanh_approx(h), h);
+}
 
 struct TileInfo {
   int e, row0, rows_valid, n0;
@@ -109,11 +118,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = g.E;
 
-  // ---- per-expert tile counts from the segment offsets
-  for (int e = tid; e < E; e += NTHREADS) {
-    const int cnt = g.offsets[e + 1] - g.offsets[e];
-    s_mt[e] = cnt > 0 ? (cnt + C::TILE_M - 1) / C::TILE_M : 0;
-  }
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -135,6 +139,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (MODE == MODE_SWIGLU) tma_prefetch_desc(&tmB3);
+  }
+  // the prologue above overlaps the predecessor's tail; its outputs (the
+  // grouped rows and their segment offsets) are read only from here on
+  pdl_wait();
+  // ---- per-expert tile counts from the segment offsets
+  for (int e = tid; e < E; e += NTHREADS) {
+    const int cnt = g.offsets[e + 1] - g.offsets[e];
+    s_mt[e] = cnt > 0 ? (cnt + C::TILE_M - 1) / C::TILE_M : 0;
   }
   __syncthreads();
   if (tid == 0) {
@@ -335,6 +347,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (tid == 0) pdl_trigger();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -381,8 +394,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
   const long long mt_bound = (rows_bound + Cfg<MT>::TILE_M - 1) / Cfg<MT>::TILE_M + g.E;
   const long long tiles_bound = mt_bound * g.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(num_sms, std::max<long long>(1, tiles_bound)));
-  kern<<<grid, NTHREADS, smem, st>>>(a, b, b3, g);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), static_cast<size_t>(smem), st, 1, a, b, b3, g);
 }
 
 }  // namespace

@@ -10,6 +10,34 @@
 
 namespace moe {
 
+// Launch `kern` on `st` with programmatic stream serialisation (it may start
+// while the previous kernel on the stream finishes; the kernel calls
+// pdl_wait() before reading that kernel's outputs).  cluster_y > 1 adds a
+// (1, cluster_y, 1) thread-block cluster.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_y, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  unsigned n = 1;
+  if (cluster_y > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = cluster_y;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kMaxExperts = 128;  // largest E the kernels support
 constexpr int kMaxTopK = 16;      // largest k the kernels support
 
@@ -17,10 +45,11 @@ constexpr int kMaxTopK = 16;      // largest k the kernels support
 // Every region starts on a 256-byte boundary.
 struct WsLayout {
   size_t err;        // int32 error word (+ padding)
-  size_t disp_ctrl;  // int32 ticket + int32 status[nblk]   (cleared per dispatch)
+  size_t disp_ctrl;  // int32 ticket, status[nblk], done (self-resetting; zero at first use)
   size_t disp_agg;   // int32 [nblk][E] per-block expert histograms
   size_t disp_incl;  // int32 [nblk][E] inclusive prefixes
   size_t idx, w, pos;        // [T,k] int32 / fp32 / int32
+  size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
   size_t counts, offsets;    // [E], [E+1] int32
   size_t dropped;            // int64
   size_t x_perm;             // [R,d] dtype
@@ -71,7 +100,8 @@ struct DispatchParams {
   int32_t* counts;
   int32_t* offsets;
   long long* dropped;
-  int* ctrl;       // ticket + status[nblk]
+  int* ctrl;       // ticket, status[nblk], done counter
+  int clear_ctrl;  // 1: zero ctrl before the kernel; 0: it is zero already (the last block resets it)
   int* agg;        // [nblk][E]
   int* incl;       // [nblk][E]
   int nblk;
@@ -88,6 +118,7 @@ struct GatherParams {
   int T, k, d, E;
   void* x_perm;
   int32_t* row_token;
+  int32_t* row_of;  // [T,k] out (optional): grouped row of each assignment, -1 if dropped
   int elem_bytes;
   long long rows_alloc;  // rows of x_perm
   int* err;
@@ -114,6 +145,7 @@ cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st);
 
 struct CombineParams {
   const float* y_perm;
+  const int32_t* row_of;  // [T,k] grouped rows (-1 dropped); when set, idx/pos/offsets are not read
   const int32_t* idx;
   const float* w;
   const int32_t* pos;

@@ -33,12 +33,13 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
     return at;
   };
   L.err = take(sizeof(int));
-  L.disp_ctrl = take(sizeof(int) * (1 + L.nblk_dispatch));
+  L.disp_ctrl = take(sizeof(int) * (2 + L.nblk_dispatch));
   L.disp_agg = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
   L.disp_incl = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
   L.idx = take(sizeof(int32_t) * Tk);
   L.w = take(sizeof(float) * Tk);
   L.pos = take(sizeof(int32_t) * Tk);
+  L.row_of = take(sizeof(int32_t) * Tk);
   L.counts = take(sizeof(int32_t) * s.E);
   L.offsets = take(sizeof(int32_t) * (s.E + 1));
   L.dropped = take(sizeof(long long));
@@ -136,7 +137,7 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g
 static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x,
                                   int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
                                   void* x_perm, int32_t* row_token, void* ws, const WsLayout& L,
-                                  cudaStream_t st, int stall_block = -1) {
+                                  cudaStream_t st, int stall_block = -1, int32_t* row_of = nullptr) {
   DispatchParams dp{};
   dp.idx = idx;
   dp.T = static_cast<int>(shape->T);
@@ -148,6 +149,7 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int
   dp.offsets = offsets;
   dp.dropped = reinterpret_cast<long long*>(dropped);
   dp.ctrl = at<int>(ws, L.disp_ctrl);
+  dp.clear_ctrl = 0;
   dp.agg = at<int>(ws, L.disp_agg);
   dp.incl = at<int>(ws, L.disp_incl);
   dp.nblk = L.nblk_dispatch;
@@ -166,6 +168,7 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int
   gp.E = shape->E;
   gp.x_perm = x_perm;
   gp.row_token = row_token;
+  gp.row_of = row_of;
   gp.elem_bytes = static_cast<int>(dtype_bytes(shape->dtype));
   gp.rows_alloc = L.rows;
   gp.err = at<int>(ws, L.err);
@@ -250,9 +253,11 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const void* x_p
 
 static moe_status_t combine_impl(const moe_shape_t* shape, long long rows, const float* y_perm, const int32_t* idx,
                                  const float* w, const int32_t* pos, const int32_t* offsets, const void* residual,
-                                 void* out, float* moe_out, int* err, cudaStream_t st) {
+                                 void* out, float* moe_out, int* err, cudaStream_t st,
+                                 const int32_t* row_of = nullptr) {
   CombineParams cp{};
   cp.y_perm = y_perm;
+  cp.row_of = row_of;
   cp.idx = idx;
   cp.w = w;
   cp.pos = pos;
@@ -307,10 +312,6 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   if (shape->T > 0 && (!aligned16(x) || !aligned16(out) || (moe_out && !aligned16(moe_out))))
     return MOE_ERR_UNSUPPORTED;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
-  if (stage_events != nullptr) {
-    for (int i = 0; i < 6; ++i)
-      if (stage_events[i] == nullptr) return MOE_ERR_INVALID_ARG;
-  }
 
   const WsLayout L = ws_layout(*shape, C);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -323,7 +324,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     if (cs == cudaStreamCaptureStatusActive) rec_flags = cudaEventRecordExternal;
   }
   auto mark = [&](int i) -> moe_status_t {
-    if (stage_events == nullptr) return MOE_OK;
+    if (stage_events == nullptr || stage_events[i] == nullptr) return MOE_OK;
     return cuda_status(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, rec_flags));
   };
   if (idx == nullptr) idx = at<int32_t>(ws, L.idx);
@@ -336,8 +337,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   if ((st = mark(0)) != MOE_OK) return st;
   if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, nullptr, stats, stream)) != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
+  int32_t* row_of = at<int32_t>(ws, L.row_of);
   if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
-                          s)) != MOE_OK)
+                          s, -1, row_of)) != MOE_OK)
     return st;
   if ((st = mark(2)) != MOE_OK) return st;
   float* y_perm = at<float>(ws, L.y_perm);
@@ -365,8 +367,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     if ((st = mark(3)) != MOE_OK) return st;
   }
   if ((st = mark(4)) != MOE_OK) return st;
-  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, out, moe_out, at<int>(ws, L.err), s)) !=
-      MOE_OK)
+  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, out, moe_out, at<int>(ws, L.err), s,
+                        row_of)) != MOE_OK)
     return st;
   return mark(5);
 }

@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
   int* cnt = reinterpret_cast<int*>(cn2 + NC);    // [2]
   const TX* x = static_cast<const TX*>(p.x);
 
+  pdl_wait();  // tokens (and weights) may be the predecessor's output
   // ---- stage the router weights, transposed, with 4-byte asynchronous
   // copies (all in flight at once); zero rows and tail padding
   for (int i = tid; i < d * NC; i += WT) {
@@ -213,6 +214,7 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
     __syncwarp();
   }
 
+  pdl_trigger();
   if (p.stats) flush_stats(p, cnt, lane, n_recomputed, n_near);
 }
 
@@ -231,8 +233,7 @@ cudaError_t launch_warp(const RouterParams& p, const WarpPlan& q, int smem_bytes
   auto kern = router_warp_kernel<TX, NC, TW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, WT, smem_bytes, st>>>(p, q);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(WT), static_cast<size_t>(smem_bytes), st, 1, p, q);
 }
 
 // The warp kernel, for nc <= 16 when the transposed weights fit in shared

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
   const int ch0 = rank * q.nch_per;
   const int nloc = max(0, min(q.nch, ch0 + q.nch_per) - ch0);
 
+  pdl_wait();  // tokens (and weights) may be the predecessor's output
   float sq[NV];
   float wsq = 0.f;  // sum of W^2 of column (tid mod NCP) over this CTA's rows
 #pragma unroll
@@ -217,6 +218,7 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
       for (int c = 0; c < 4; ++c) acc[m][c] += cacc[m][c];
   }
   cp_async_wait_all();
+  pdl_trigger();
   __syncthreads();  // the slice buffers are dead: the partial-logit tile may alias them
 
   // -------- park this CTA's partial logits and norms in shared memory
@@ -332,18 +334,21 @@ cudaError_t launch_one(const RouterParams& p, const TiledPlan& q, long long tile
   if (e != cudaSuccess) return e;
   if (q.KS > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
     return e;
+  // a cluster of KS CTAs along y (also for KS = 1, so the cluster API sees a cluster)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(q.KS), 1);
   cfg.blockDim = dim3(RT, 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(G::SMEM);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = static_cast<unsigned>(q.KS);
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p, q);
 }
 

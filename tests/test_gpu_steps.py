@@ -139,11 +139,13 @@ def test_dispatch_bounded_wait_reports_timeout():
     assert api.get_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("T,k,E,C", [(20000, 2, 16, 2600), (150000, 2, 8, 40000), (700, 3, 5, 300)],
-                         ids=["40_small_tiles", "large_tiles", "one_tile_E5"])
+@pytest.mark.parametrize("T,k,E,C", [(20000, 2, 16, 2600), (150000, 2, 8, 40000), (700, 3, 5, 300),
+                                     (2000, 2, 128, 40), (5000, 2, 8, 1000)],
+                         ids=["40_small_tiles", "large_tiles", "single_cta_E5", "single_cta_E128", "five_tiles"])
 def test_dispatch_many_tiles(T, k, E, C):
-    """Dispatch across more tiles than the 32-tile look-back window (1024- and
-    4096-assignment tiles): slots, counts, offsets and drops bit-exact."""
+    """Dispatch on one CTA (up to 8192 assignments) and across tiles, more
+    than the 32-tile look-back window included (1024- and 4096-assignment
+    tiles): slots, counts, offsets and drops bit-exact."""
     g = torch.Generator().manual_seed(T)
     logits = torch.randn(T, E, generator=g) + torch.linspace(1.0, -1.0, E)
     idx = logits.topk(k, dim=1).indices.int()
@@ -157,10 +159,13 @@ def test_dispatch_many_tiles(T, k, E, C):
     assert api.get_device_error(d["ws"]) == 0
 
 
-def test_dispatch_out_of_range_expert_is_reported():
+@pytest.mark.parametrize("T", [300, 9000], ids=["single_cta", "tiled"])
+def test_dispatch_out_of_range_expert_is_reported(T):
     """An expert id outside [0, E) takes no slot and sets MOE_ERR_BOUNDS; the
-    other assignments are dispatched as if it were absent."""
-    T, k, E, C = 300, 2, 6, 200
+    other assignments are dispatched as if it were absent (both the one-CTA
+    kernel and the tiled look-back kernel)."""
+    k, E = 2, 6
+    C = T * k // 3
     g = torch.Generator().manual_seed(9)
     idx = torch.stack([torch.randperm(E, generator=g)[:k] for _ in range(T)]).int()
     idx[17, 1] = E      # one past the last expert
