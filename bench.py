@@ -5,8 +5,10 @@
 
 One step = one whole layer forward (router, top-k, capacity dispatch + gather,
 expert GEMMs, combine) over one batch of seeded synthetic tokens already
-resident in HBM.  L2 is flushed (256 MiB write) between timed steps, outside
-the measured events.  Prints one JSON line.
+resident in HBM, issued through the C ABI (moe_forward_timed).  The timed
+steps are replayed as CUDA graphs (--eager: launched from the host); L2 is
+flushed (256 MiB write) between timed steps, outside the measured events.
+Prints one JSON line.
 
 --impl reference times the fp64 CPU oracle instead (the reference arm of this
 benchmark), on the host cores, each step a bounded sub-batch of the workload.
