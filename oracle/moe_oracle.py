@@ -279,3 +279,58 @@ def near_ties(H: np.ndarray, k: int, thresh: float = 1e-4) -> dict:
     for j in range(m - 1):
         inner |= (s[:, j] - s[:, j + 1]) < thresh
     return dict(boundary=np.nonzero(boundary)[0], any_adjacent=np.nonzero(inner)[0])
+
+
+# --------------------------------------------------------------------------
+# routing diagnostics and the auxiliary load-balancing loss
+# --------------------------------------------------------------------------
+
+def routing_stats(H: np.ndarray, idx: np.ndarray, counts: np.ndarray, dropped: int) -> dict:
+    """Routing diagnostics of one batch and the auxiliary load-balancing loss.
+
+    [P1] "Mathematical Formulation": L_aux = N * sum_i f_i * P_i, f_i the
+    fraction of the batch dispatched to expert i (a hard count), P_i the mean
+    routing probability of expert i over the batch; uniform routing gives
+    exactly 1.  [P1] Lab 2 takes P from the full softmax of the router logits.
+    [P4] s4 states the same loss with the coefficient alpha left to the
+    trainer.  [P2] Level 2 asks to report the probability mass and the
+    realised loads side by side, with overflow, utilisation and a stated
+    imbalance measure.
+
+    Readings (top-k): f_i counts every selected assignment (t, r) with
+    idx[t,r] = i before the capacity cut, divided by T*k, so f sums to 1; P
+    is the mean over tokens of softmax(H[t]) over all E experts (the noisy
+    logits when noise is used).
+
+    H [T,E] logits, idx [T,k] selected experts, counts [E] kept assignments
+    (after capacity), dropped = assignments over capacity.
+    Returns f [E], P [E], aux_loss, entropy (mean over tokens of
+    -sum_e p ln p, nats), load_cv (population std / mean of the
+    pre-capacity loads), kept_cv (same for counts), utilisation (fraction of
+    experts with a kept assignment), overflow (dropped / (T*k)).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    T, E = H.shape
+    idx = np.asarray(idx, dtype=np.int64)
+    k = idx.shape[1]
+    counts = np.asarray(counts, dtype=np.float64)
+    if T == 0:
+        zero = np.zeros(E)
+        return dict(f=zero, P=zero, aux_loss=0.0, entropy=0.0, load_cv=0.0, kept_cv=0.0, utilisation=0.0,
+                    overflow=0.0, loads=zero)
+    p = np.exp(H - H.max(axis=1, keepdims=True))
+    p = p / p.sum(axis=1, keepdims=True)
+    P = p.mean(axis=0)
+    loads = np.bincount(idx.reshape(-1), minlength=E).astype(np.float64)
+    f = loads / float(T * k)
+    aux = float(E) * float(np.sum(f * P))
+    with np.errstate(divide="ignore", invalid="ignore"):
+        plogp = np.where(p > 0.0, p * np.log(p), 0.0)
+    entropy = float(-plogp.sum(axis=1).mean())
+
+    def cv(v):
+        m = v.mean()
+        return float(np.sqrt(((v - m) ** 2).mean()) / m) if m > 0 else 0.0
+
+    return dict(f=f, P=P, aux_loss=aux, entropy=entropy, load_cv=cv(loads), kept_cv=cv(counts),
+                utilisation=float((counts > 0).sum()) / E, overflow=float(dropped) / float(T * k), loads=loads)

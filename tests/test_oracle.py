@@ -339,3 +339,99 @@ def test_workload_generator_is_deterministic():
             assert torch.equal(a[key], b[key])
     s = W.make_inputs(W.WORKLOADS["switch_top1"].scaled(64))
     np.testing.assert_allclose(s["b_g"].numpy()[:3], [0.0, 2 * math.log(0.5), 2 * math.log(1 / 3)], rtol=1e-6)
+
+
+# ----------------------------------------------------------------------------
+# routing diagnostics and the auxiliary load-balancing loss
+# ----------------------------------------------------------------------------
+
+def _softmax_rows(H):
+    z = np.exp(H - H.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def test_aux_loss_is_one_for_uniform_routing():
+    """[P1] Mathematical Formulation: uniform f and P give L_aux = 1 exactly;
+    uniform probabilities have entropy ln E; equal loads have zero CV."""
+    T, E, k = 24, 6, 2
+    H = np.zeros((T, E))
+    idx = np.array([[t % E, (t + 1) % E] for t in range(T)])
+    counts = np.full(E, T * k // E)
+    st = O.routing_stats(H, idx, counts, 0)
+    assert st["aux_loss"] == pytest.approx(1.0, abs=1e-15)
+    assert st["entropy"] == pytest.approx(math.log(E), abs=1e-12)
+    assert st["load_cv"] == 0.0 and st["kept_cv"] == 0.0
+    assert st["utilisation"] == 1.0 and st["overflow"] == 0.0
+    np.testing.assert_allclose(st["f"], 1.0 / E)
+    np.testing.assert_allclose(st["P"], 1.0 / E)
+
+
+def test_aux_loss_is_E_for_full_collapse():
+    """Every token routed to one expert with probability ~1: f = P = e_0, so
+    L_aux -> E and the per-token entropy -> 0."""
+    T, E = 50, 8
+    H = np.full((T, E), -80.0)
+    H[:, 0] = 80.0
+    idx = np.zeros((T, 1), dtype=np.int64)
+    st = O.routing_stats(H, idx, np.array([T] + [0] * (E - 1)), 0)
+    assert st["aux_loss"] == pytest.approx(E, rel=1e-12)
+    assert st["entropy"] < 1e-60
+    assert st["utilisation"] == 1.0 / E
+
+
+@pytest.mark.parametrize("seed", [3, 4, 5])
+def test_aux_loss_detects_collapse(seed):
+    """[P1] Lab 2: logits N(0, 0.5^2) per expert, top-1 routing; adding 5 to
+    expert 0's logit (collapse) lifts the loss above 1.5, the balanced router
+    stays below 1.5 (our seeds, the lab's thresholds)."""
+    rng = np.random.default_rng(seed)
+    T, E = 200, 6
+    base = rng.standard_normal((T, E)) * 0.5
+    out = {}
+    for name, bias in (("balanced", 0.0), ("collapsed", 5.0)):
+        H = base.copy()
+        H[:, 0] += bias
+        idx = O.topk(H, 1)
+        d = O.dispatch(idx, E, T)
+        out[name] = O.routing_stats(H, idx, d["counts"], d["dropped"])
+    assert out["balanced"]["aux_loss"] < 1.5 < out["collapsed"]["aux_loss"]
+    assert out["collapsed"]["f"][0] > 0.9
+    assert out["collapsed"]["load_cv"] > out["balanced"]["load_cv"]
+
+
+def test_routing_stats_brute_force_and_token_order():
+    """f, P, the loss and the entropy against element-by-element loops on a
+    small batch with top-3 routing and capacity drops; the statistics do not
+    depend on the order of the tokens."""
+    rng = np.random.default_rng(11)
+    T, E, k, C = 13, 5, 3, 6
+    H = rng.standard_normal((T, E)) * 2.0
+    idx = O.topk(H, k)
+    d = O.dispatch(idx, E, C)
+    st = O.routing_stats(H, idx, d["counts"], d["dropped"])
+    f = [0.0] * E
+    P = [0.0] * E
+    ent = 0.0
+    for t in range(T):
+        m = max(H[t])
+        ex = [math.exp(H[t, e] - m) for e in range(E)]
+        s = sum(ex)
+        for e in range(E):
+            P[e] += ex[e] / s / T
+            ent -= (ex[e] / s) * math.log(ex[e] / s) / T
+        for r in range(k):
+            f[idx[t, r]] += 1.0 / (T * k)
+    np.testing.assert_allclose(st["f"], f, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(st["P"], P, rtol=0, atol=1e-15)
+    assert st["aux_loss"] == pytest.approx(E * sum(a * b for a, b in zip(f, P)), abs=1e-14)
+    assert st["entropy"] == pytest.approx(ent, abs=1e-14)
+    # f is taken before the capacity cut: the drops change the kept CV, not f
+    assert d["dropped"] > 0
+    loads = np.array(f) * T * k
+    assert st["load_cv"] == pytest.approx(float(np.std(loads) / np.mean(loads)), abs=1e-14)
+    assert st["overflow"] == pytest.approx(d["dropped"] / (T * k))
+    perm = rng.permutation(T)
+    st2 = O.routing_stats(H[perm], idx[perm], d["counts"], d["dropped"])
+    for key in ("f", "P"):
+        np.testing.assert_allclose(st2[key], st[key], atol=1e-15)
+    assert st2["aux_loss"] == pytest.approx(st["aux_loss"], abs=1e-14)
