@@ -8,7 +8,10 @@ expert GEMMs, combine) over one batch of seeded synthetic tokens already
 resident in HBM, issued through the C ABI (moe_forward_timed).  The timed
 steps are replayed as CUDA graphs (--eager: launched from the host); L2 is
 flushed (256 MiB write) between timed steps, outside the measured events.
-Prints one JSON line.
+Prints one JSON line.  Besides the layer, the line carries `routing_stats`:
+the time of one moe_routing_stats call over the same batch (routing
+diagnostics and auxiliary load-balancing loss; L2 flushed before each call)
+and the values it returned.
 
 --impl reference times the fp64 CPU oracle instead (the reference arm of this
 benchmark), on the host cores, each step a bounded sub-batch of the workload.
@@ -316,7 +319,7 @@ def run_ours(a):
         sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
         return [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
                 P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), P(out),
-                None, None, None, None, P(counts), None, P(dropped), None, P(ws), ws.numel(), sptr]
+                None, None, None, None, P(counts), None, P(dropped), None, None, P(ws), ws.numel(), sptr]
 
     # the timed steps run as CUDA graphs of up to GRAPH_STEPS steps each (every
     # step the same C-ABI call, moe_forward_timed, its launches replayed
@@ -464,6 +467,42 @@ def run_ours(a):
     e2e = {"value": w.T * n_e2e * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
+    # ---------------- routing diagnostics + aux loss of the same batch (moe_routing_stats,
+    # a separate call after the layer): kernel time with L2 flushed before each call
+    logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
+    idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+    fa = fwd_args()
+    fa[15], fa[22] = P(idx_t), P(logits)
+    _lib.check(lib.moe_forward(*fa), "moe_forward")
+    st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def stats_call():
+        _lib.check(lib.moe_routing_stats(ctypes.byref(shape), P(logits), P(idx_t), P(counts), P(dropped),
+                                         P(st_out[0]), P(st_out[1]), P(st_out[2]), P(ws), ws.numel(), sptr),
+                   "moe_routing_stats")
+
+    for _ in range(3):
+        stats_call()
+    n_st = 50
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_st)]
+    for i in range(n_st):
+        flush.zero_()
+        sev[i][0].record(stream)
+        stats_call()
+        sev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if api.get_device_error(ws) != 0:
+        raise RuntimeError("device-side error in moe_routing_stats")
+    st_ms = statistics.mean(s.elapsed_time(e) for s, e in sev)
+    st_bytes = w.T * w.E * 4 + w.T * w.k * 4  # logits + top-k table, read once
+    summ = dict(zip(api.STATS_SUMMARY, st_out[2].tolist()))
+    routing_stats = {"us_per_call": st_ms * 1e3, "algorithmic_bytes": st_bytes,
+                     "achieved_gbs": st_bytes / (st_ms / 1e3) / 1e9,
+                     "frac_hbm": st_bytes / (st_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                     "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
+                     "overflow": summ["overflow"]}
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -485,7 +524,7 @@ def run_ours(a):
             "stage_ms": {n: statistics.mean(v) for n, v in zip(
                 ["router_dispatch_gather", "expert_gemm1", "expert_gemm2_combine"], stage_ms)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * a.steps,
-            "clocks": sampler.summary()}
+            "clocks": sampler.summary(), "routing_stats": routing_stats}
     print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -211,6 +211,9 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const floa
  *   idx, w, pos [T,k], counts [E], offsets [E+1], dropped [1], stats [2]:
  *     optional outputs (NULL = keep them in the workspace only; stats as
  *     in moe_route, added to)
+ *   logits [T,E] fp32 | NULL  optional output: the router's (noisy) logits,
+ *     as in moe_route; with idx, counts and dropped it feeds
+ *     moe_routing_stats
  *   ws, ws_bytes  workspace of moe_workspace_size(shape, C) bytes */
 MOE_API moe_status_t moe_forward(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
                          const void* x, const float* W_g, const float* b_g,
@@ -218,7 +221,7 @@ MOE_API moe_status_t moe_forward(const moe_shape_t* shape, double capacity_facto
                          const void* W3, const void* W2, const float* b1, const float* b2,
                          void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
                          int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
-                         void* ws, size_t ws_bytes, void* stream);
+                         float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward, recording up to six CUDA events (cudaEvent_t, created by the
  * caller) on `stream` at the stage boundaries, so each stage can be timed
@@ -238,7 +241,36 @@ MOE_API moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity
                                        const void* W3, const void* W2, const float* b1, const float* b2,
                                        void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
                                        int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
-                                       void* ws, size_t ws_bytes, void* stream, void* const* stage_events);
+                                       float* logits, void* ws, size_t ws_bytes, void* stream,
+                                       void* const* stage_events);
+
+/* Routing diagnostics of one batch and the auxiliary load-balancing loss
+ * ("Mixture-of-Experts Sparse Model Scaling", Mathematical Formulation and
+ * Lab 2: L_aux = E * sum_e f_e P_e, uniform routing gives 1; "LLM part 09",
+ * s4; "Mixture-of-experts Models", Level 3 wants the probability mass,
+ * the realised loads, overflow and utilisation side by side).
+ *   logits   [T,E] fp32       router logits (moe_route / moe_forward output)
+ *   idx      [T,k] int32      selected experts
+ *   counts   [E]   int32      kept assignments per expert (after capacity)
+ *   dropped  [1]   int64      assignments over capacity
+ *   f        [E]   fp64 out   routed (pre-capacity) load of e over T*k
+ *   P        [E]   fp64 out   mean over tokens of softmax(logits[t])[e]
+ *   summary  [6]   fp64 out   [0] aux loss E * sum_e f_e P_e
+ *                             [1] mean router entropy -sum_e p ln p (nats)
+ *                             [2] routed-load imbalance: population std /
+ *                                 mean of the pre-capacity loads
+ *                             [3] the same for the kept counts
+ *                             [4] utilisation: fraction of experts with a
+ *                                 kept assignment
+ *                             [5] overflow: dropped / (T*k)
+ *   ws, ws_bytes  the workspace of moe_workspace_size(shape, C) for any C
+ * T = 0 gives all zeros.  One kernel; the softmax is taken in fp32, every
+ * sum in fp64 in a fixed order, so results are deterministic.  An expert id
+ * outside [0,E) is counted nowhere and sets MOE_ERR_BOUNDS in the error
+ * word.  Calls that share a workspace must be ordered on one stream. */
+MOE_API moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, const int32_t* idx,
+                                       const int32_t* counts, const int64_t* dropped, double* f, double* P,
+                                       double* summary, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, reads the workspace's device error word, clears it,
  * and returns it as a status (MOE_OK when no device-side error was recorded

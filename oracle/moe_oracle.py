@@ -13,14 +13,17 @@ the source pages it restates.  The pages are cited by title and section:
 
   [P1] "Mixture-of-Experts Sparse Model Scaling" (glossary page), sections
        "Mathematical Formulation", "Advanced Theory & Extensions", and the
-       "Practical Labs" appendix (Lab 1 top-k router, Lab 3 capacity).
+       "Practical Labs" appendix (Lab 1 top-k router, Lab 2 load-balancing
+       loss, Lab 3 capacity).
   [P2] "Mixture-of-experts Models" (book chapter), Level 2 "Router scores
        become a sparse dispatch decision", "Top-k selection has ties",
-       "Capacity limits make dispatch observable" (Figure 44.4).
+       "Capacity limits make dispatch observable" (Figure 44.4); Level 3
+       "Load balancing has probability, assignment, and quality diagnostics".
   [P3] "Scaling Capacity via Sparse Mixture of Experts (MoE) Architectures",
        the SimpleRouter listing.
   [P4] "LLM part 09: Sparse Mixture-of-Experts (MoE)", section 1 (output
-       equation), section 2 (noisy top-k gating), section 3 (capacity).
+       equation), section 2 (noisy top-k gating), section 3 (capacity),
+       section 4 (auxiliary load-balancing loss).
   [P5] "3D mixture-of-experts routing lab", the "Capacity" card.
 
 Readings taken where the pages are silent or disagree:
@@ -293,9 +296,9 @@ def routing_stats(H: np.ndarray, idx: np.ndarray, counts: np.ndarray, dropped: i
     routing probability of expert i over the batch; uniform routing gives
     exactly 1.  [P1] Lab 2 takes P from the full softmax of the router logits.
     [P4] s4 states the same loss with the coefficient alpha left to the
-    trainer.  [P2] Level 2 asks to report the probability mass and the
-    realised loads side by side, with overflow, utilisation and a stated
-    imbalance measure.
+    trainer.  [P2] Level 3 (load-balancing diagnostics) asks for the
+    probability mass and the realised loads together, with overflow,
+    utilisation and a named imbalance measure.
 
     Readings (top-k): f_i counts every selected assignment (t, r) with
     idx[t,r] = i before the capacity cut, divided by T*k, so f sums to 1; P

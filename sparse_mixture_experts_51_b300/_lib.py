@@ -43,10 +43,11 @@ SIGNATURES = {
     "moe_expert_ffn": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       ctypes.c_size_t, _P]),
     "moe_combine": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "moe_forward": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 20
+    "moe_forward": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 21
                     + [ctypes.c_size_t, _P]),
-    "moe_forward_timed": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 20
+    "moe_forward_timed": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 21
                           + [ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_void_p)]),
+    "moe_routing_stats": (ctypes.c_int, [_SHAPE] + [_P] * 8 + [ctypes.c_size_t, _P]),
     "moe_get_device_error": (ctypes.c_int, [_P, _P]),
     "moe_testing_dispatch_stalled": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 7
                                      + [ctypes.c_int32, _P, ctypes.c_size_t, _P]),

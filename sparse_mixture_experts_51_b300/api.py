@@ -114,6 +114,37 @@ def dispatch(idx: torch.Tensor, x: torch.Tensor, E: int, C: int, d_ff: int = 64,
     return out
 
 
+STATS_SUMMARY = ("aux_loss", "entropy", "load_cv", "kept_cv", "utilisation", "overflow")
+
+
+def routing_stats(logits: torch.Tensor, idx: torch.Tensor, counts: torch.Tensor, dropped: torch.Tensor,
+                  ws: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Routing diagnostics and the auxiliary load-balancing loss of one batch.
+
+    Returns device tensors: f [E] fp64 (routed load over T*k, before the
+    capacity cut), P [E] fp64 (mean full-softmax probability) and summary [6]
+    fp64 in the order of STATS_SUMMARY.  ``ws`` is any workspace of the same
+    T, k and E (a fresh one is made if None)."""
+    T, E = logits.shape
+    k = idx.shape[1]
+    shape = shape_of(T, 64, E, k, 64, torch.float32, MOE_ACT_GELU)
+    dev = logits.device
+    if ws is None:
+        ws = new_workspace(shape, 0, dev)
+    out = dict(f=torch.empty(E, dtype=torch.float64, device=dev), P=torch.empty(E, dtype=torch.float64, device=dev),
+               summary=torch.empty(len(STATS_SUMMARY), dtype=torch.float64, device=dev))
+    st = _lib.load().moe_routing_stats(ctypes.byref(shape), _ptr(logits), _ptr(idx), _ptr(counts), _ptr(dropped),
+                                       _ptr(out["f"]), _ptr(out["P"]), _ptr(out["summary"]), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _lib.check(st, "moe_routing_stats")
+    return out
+
+
+def stats_summary(stats: dict) -> dict:
+    """The summary tensor of routing_stats as named Python floats (synchronises)."""
+    return dict(zip(STATS_SUMMARY, stats["summary"].tolist()))
+
+
 def expert_ffn(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor, T: int, k: int,
                C: int, act, W3=None, b1=None, b2=None, ws: Optional[torch.Tensor] = None, stream=None):
     """Every expert's FFN over its rows of x_perm.  Returns y_perm fp32 [max_rows, d]."""
@@ -148,8 +179,10 @@ class MoELayer:
 
     ``layer(x, eps=None)`` runs the whole forward pass (moe_forward) on the
     current stream and returns the output tensor; ``layer.last`` keeps the
-    routing outputs of the call (idx, w, pos, counts, offsets, dropped,
-    stats) when ``keep_routing`` is set.
+    routing outputs of the call (idx, w, pos, counts, offsets, dropped, and
+    the router logits) when ``keep_routing`` is set, and
+    ``layer.routing_stats()`` turns them into the routing diagnostics and the
+    auxiliary load-balancing loss.
     """
 
     def __init__(self, W_g, W1, W2, k: int, act, W3=None, b_g=None, W_noise=None, b1=None, b2=None,
@@ -208,19 +241,29 @@ class MoELayer:
                      pos=torch.empty(T, self.k, dtype=torch.int32, device=dev),
                      counts=torch.empty(self.E, dtype=torch.int32, device=dev),
                      offsets=torch.empty(self.E + 1, dtype=torch.int32, device=dev),
-                     dropped=torch.empty(1, dtype=torch.int64, device=dev))
+                     dropped=torch.empty(1, dtype=torch.int64, device=dev),
+                     logits=torch.empty(T, self.E, dtype=torch.float32, device=dev))
         g = (lambda n: _ptr(r[n])) if r is not None else (lambda n: None)
         st = _lib.load().moe_forward(
             ctypes.byref(shape), float(self.capacity_factor or 0.0), int(C if self.C_fixed is not None else -1),
             _ptr(x), _ptr(self.W_g), _ptr(self.b_g), _ptr(self.W_noise), _ptr(eps), _ptr(self.W1), _ptr(self.W3),
             _ptr(self.W2), _ptr(self.b1), _ptr(self.b2), _ptr(out), _ptr(moe), g("idx"), g("w"), g("pos"),
-            g("counts"), g("offsets"), g("dropped"), _ptr(stats), _ptr(ws), ws.numel(), _stream(stream))
+            g("counts"), g("offsets"), g("dropped"), _ptr(stats), g("logits"), _ptr(ws), ws.numel(),
+            _stream(stream))
         _lib.check(st, "moe_forward")
         if r is not None:
             r["C"] = C
             r["moe"] = moe
+            r["ws"] = ws
         self.last = r
         return out
+
+    def routing_stats(self, stream=None) -> dict:
+        """Routing diagnostics of the last call (see routing_stats); needs keep_routing."""
+        r = self.last
+        if r is None:
+            raise RuntimeError("no routing outputs kept: call the layer with keep_routing=True first")
+        return routing_stats(r["logits"], r["idx"], r["counts"], r["dropped"], ws=r["ws"], stream=stream)
 
 
 class CapturedForward:
@@ -265,4 +308,5 @@ def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=No
 
 
 __all__ = ["capacity", "max_rows", "workspace_size", "new_workspace", "get_device_error", "route", "dispatch",
-           "expert_ffn", "combine", "forward", "MoELayer", "CapturedForward", "MoeError", "shape_of"]
+           "expert_ffn", "combine", "forward", "routing_stats", "stats_summary", "STATS_SUMMARY", "MoELayer",
+           "CapturedForward", "MoeError", "shape_of"]

@@ -40,6 +40,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 constexpr int kMaxExperts = 128;  // largest E the kernels support
 constexpr int kMaxTopK = 16;      // largest k the kernels support
+constexpr int kStatsMaxBlocks = 148;  // blocks of the routing-stats kernel (one wave)
 
 // Workspace carve-up shared by moe_forward / moe_dispatch / moe_expert_ffn.
 // Every region starts on a 256-byte boundary.
@@ -48,6 +49,9 @@ struct WsLayout {
   size_t disp_ctrl;  // int32 ticket, status[nblk], done (self-resetting; zero at first use)
   size_t disp_agg;   // int32 [nblk][E] per-block expert histograms
   size_t disp_incl;  // int32 [nblk][E] inclusive prefixes
+  size_t stats_ticket;  // int32 last-block ticket of moe_routing_stats (self-resetting)
+  size_t stats_part;    // fp64 [kStatsMaxBlocks][E+1] per-block sums of p (and entropy)
+  size_t stats_load;    // int32 [kStatsMaxBlocks][E] per-block routed loads
   size_t idx, w, pos;        // [T,k] int32 / fp32 / int32
   size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
   size_t counts, offsets;    // [E], [E+1] int32
@@ -159,5 +163,23 @@ struct CombineParams {
   int* err;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st);
+
+struct StatsParams {
+  const float* logits;     // [T,E]
+  const int32_t* idx;      // [T,k]
+  const int32_t* counts;   // [E] kept per expert
+  const long long* dropped;
+  long long T;
+  int E, k;
+  double* f;        // [E] out
+  double* P;        // [E] out
+  double* summary;  // [6] out
+  double* part;     // [kStatsMaxBlocks][E+1]
+  int* load_part;   // [kStatsMaxBlocks][E]
+  int* ticket;
+  int* err;
+};
+int stats_blocks(long long T);
+cudaError_t launch_routing_stats(const StatsParams& p, cudaStream_t st);
 
 }  // namespace moe

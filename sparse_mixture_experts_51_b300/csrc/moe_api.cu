@@ -36,6 +36,9 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.disp_ctrl = take(sizeof(int) * (2 + L.nblk_dispatch));
   L.disp_agg = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
   L.disp_incl = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
+  L.stats_ticket = take(sizeof(int));
+  L.stats_part = take(sizeof(double) * static_cast<size_t>(kStatsMaxBlocks) * (s.E + 1));
+  L.stats_load = take(sizeof(int) * static_cast<size_t>(kStatsMaxBlocks) * s.E);
   L.idx = take(sizeof(int32_t) * Tk);
   L.w = take(sizeof(float) * Tk);
   L.pos = take(sizeof(int32_t) * Tk);
@@ -296,8 +299,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
                                  const void* x, const float* W_g, const float* b_g, const float* W_noise,
                                  const float* eps, const void* W1, const void* W3, const void* W2, const float* b1,
                                  const float* b2, void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
-                                 int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats, void* ws,
-                                 size_t ws_bytes, void* stream, void* const* stage_events) {
+                                 int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
+                                 float* logits, void* ws, size_t ws_bytes, void* stream,
+                                 void* const* stage_events) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
   int32_t C = C_override;
@@ -335,7 +339,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   if (dropped == nullptr) dropped = at<int64_t>(ws, L.dropped);
 
   if ((st = mark(0)) != MOE_OK) return st;
-  if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, nullptr, stats, stream)) != MOE_OK) return st;
+  if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, stream)) != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   int32_t* row_of = at<int32_t>(ws, L.row_of);
   if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
@@ -377,20 +381,50 @@ moe_status_t moe_forward(const moe_shape_t* shape, double capacity_factor, int32
                          const float* W_g, const float* b_g, const float* W_noise, const float* eps, const void* W1,
                          const void* W3, const void* W2, const float* b1, const float* b2, void* out, float* moe_out,
                          int32_t* idx, float* w, int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
-                         int64_t* stats, void* ws, size_t ws_bytes, void* stream) {
+                         int64_t* stats, float* logits, void* ws, size_t ws_bytes, void* stream) {
   return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
-                      moe_out, idx, w, pos, counts, offsets, dropped, stats, ws, ws_bytes, stream, nullptr);
+                      moe_out, idx, w, pos, counts, offsets, dropped, stats, logits, ws, ws_bytes, stream, nullptr);
 }
 
 moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity_factor, int32_t C_override, const void* x,
                                const float* W_g, const float* b_g, const float* W_noise, const float* eps,
                                const void* W1, const void* W3, const void* W2, const float* b1, const float* b2,
                                void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos, int32_t* counts,
-                               int32_t* offsets, int64_t* dropped, int64_t* stats, void* ws, size_t ws_bytes,
-                               void* stream, void* const* stage_events) {
+                               int32_t* offsets, int64_t* dropped, int64_t* stats, float* logits, void* ws,
+                               size_t ws_bytes, void* stream, void* const* stage_events) {
   if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
   return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
-                      moe_out, idx, w, pos, counts, offsets, dropped, stats, ws, ws_bytes, stream, stage_events);
+                      moe_out, idx, w, pos, counts, offsets, dropped, stats, logits, ws, ws_bytes, stream,
+                      stage_events);
+}
+
+moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, const int32_t* idx,
+                               const int32_t* counts, const int64_t* dropped, double* f, double* P, double* summary,
+                               void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (counts == nullptr || dropped == nullptr || f == nullptr || P == nullptr || summary == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (logits == nullptr || idx == nullptr)) return MOE_ERR_INVALID_ARG;
+  // the stats regions precede every capacity-dependent region, so any C's workspace holds them
+  if ((st = check_ws(shape, 0, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*shape, 0);
+  StatsParams p{};
+  p.logits = logits;
+  p.idx = idx;
+  p.counts = counts;
+  p.dropped = reinterpret_cast<const long long*>(dropped);
+  p.T = shape->T;
+  p.E = shape->E;
+  p.k = shape->k;
+  p.f = f;
+  p.P = P;
+  p.summary = summary;
+  p.part = at<double>(ws, L.stats_part);
+  p.load_part = at<int>(ws, L.stats_load);
+  p.ticket = at<int>(ws, L.stats_ticket);
+  p.err = at<int>(ws, L.err);
+  return cuda_status(launch_routing_stats(p, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_get_device_error(void* ws, void* stream) {

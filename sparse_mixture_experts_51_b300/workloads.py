@@ -141,6 +141,20 @@ def make_tokens(w: Workload, seed: int) -> tuple:
     return x, eps
 
 
+def make_routing_tables(T: int, E: int, k: int, seed: int, logit_std: float = 2.0) -> dict:
+    """Arbitrary routing tables of the shapes the routing-statistics call takes.
+
+    logits [T,E] fp32 ~ N(0, logit_std^2); idx [T,k] int32 uniform in [0,E)
+    (any ids, not necessarily the top-k of the logits); counts [E] int32
+    uniform in [0, k*T/E + 1]; dropped [1] int64 uniform in [0, T*k]."""
+    g = torch.Generator().manual_seed(seed)
+    logits = _normal(g, (T, E), logit_std)
+    idx = torch.randint(0, E, (T, k), generator=g, dtype=torch.int64).to(torch.int32)
+    counts = torch.randint(0, k * T // E + 2, (E,), generator=g, dtype=torch.int64).to(torch.int32)
+    dropped = torch.randint(0, T * k + 1, (1,), generator=g, dtype=torch.int64)
+    return dict(logits=logits, idx=idx, counts=counts, dropped=dropped)
+
+
 def as_f64_numpy(t: Optional[torch.Tensor]):
     """Widen a stored tensor (fp32 or bf16) to a float64 numpy array, exactly."""
     if t is None:

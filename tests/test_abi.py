@@ -134,7 +134,7 @@ def test_forward_argument_errors(lib):
     s = _shape()
     f = P(FAKE)
     st, n = _ws(lib, s, 40)
-    args = [f, f, None, None, None, f, None, f, None, None, f, None, None, None, None, None, None, None, None]
+    args = [f, f, None, None, None, f, None, f, None, None, f, None, None, None, None, None, None, None, None, None]
     # bad capacity factor with no override
     assert lib.moe_forward(ctypes.byref(s), 0.0, -1, *args, f, n, None) == INVALID
     # a workspace sized for C=10 (40 grouped rows) is too small for cf=1.25 (C=40, 128 rows)
@@ -152,3 +152,21 @@ def test_status_strings(lib):
     for code, name in _lib.STATUS_NAMES.items():
         assert lib.moe_status_string(code).decode().startswith(name)
     assert b"unknown" in lib.moe_status_string(99)
+
+
+@no_gpu
+def test_routing_stats_argument_errors(lib):
+    s = _shape()
+    f = P(FAKE)
+    st, n = _ws(lib, s, 0)
+    # missing outputs or inputs
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, None, f, f, f, n, None) == INVALID
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, None, f, n, None) == INVALID
+    assert lib.moe_routing_stats(ctypes.byref(s), None, f, f, f, f, f, f, f, n, None) == INVALID
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, None, f, f, f, f, f, n, None) == INVALID
+    # a bad shape
+    assert lib.moe_routing_stats(ctypes.byref(_shape(k=5)), f, f, f, f, f, f, f, f, n, None) == INVALID
+    # a workspace that is missing, misaligned or too small
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, None, n, None) == WORKSPACE
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, P(FAKE + 16), n, None) == WORKSPACE
+    assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, f, n - 256, None) == WORKSPACE
