@@ -195,19 +195,41 @@ def expert(xr: np.ndarray, e: int, act: int, W1, W3, W2, b1=None, b2=None) -> np
     return y
 
 
+def shared_experts(x, act: int, W1s, W2s, W3s=None, b1s=None, b2s=None, tokens=None) -> np.ndarray:
+    """Sum of the shared experts' outputs for each token ([P1] "Advanced
+    Theory & Extensions": fine-grained designs add dedicated shared experts
+    that every token passes through unconditionally; [P1] "Real-World
+    Applications" names DeepSeek-MoE for this design).
+
+    Readings: a shared expert has the routed experts' form (``expert``) and
+    enters with weight 1 (the pages give it no gate); S shared experts are
+    summed in order s = 0..S-1.
+    W1s, W3s [S,F_s,d], W2s [S,d,F_s], b1s [S,F_s], b2s [S,d] (nn.Linear layout).
+    Returns [n,d] for the rows in ``tokens`` (all tokens when None).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    toks = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    xs = x[toks]
+    y = np.zeros_like(xs)
+    for s in range(len(W1s)):
+        y = y + expert(xs, s, act, W1s, W3s, W2s, b1s, b2s)
+    return y
+
+
 # --------------------------------------------------------------------------
 # whole layer
 # --------------------------------------------------------------------------
 
-def combine(x, idx, w, pos, expert_out, residual=True, tokens=None) -> dict:
+def combine(x, idx, w, pos, expert_out, residual=True, tokens=None, shared_out=None) -> dict:
     """Weighted combination y = sum_i G(x)_i E_i(x) over the kept assignments
     ([P4] s1; [P1] "Mathematical Formulation"; [P1] Lab 1 accumulates
     weight * expert output per token), plus the residual that carries a
     dropped token through unchanged ([P1] "Advanced Theory"; [P4] s3).
 
     expert_out[(t, r)] holds E_{idx[t,r]}(x_t) for every kept (t, r) of the
-    tokens evaluated.  Ranks are summed in order 0..k-1.
-    Returns moe [n,d] (the weighted expert sum) and out = x + moe for the
+    tokens evaluated.  Ranks are summed in order 0..k-1; ``shared_out`` [n,d]
+    (the shared experts' sum for the same rows, or None) is added after them.
+    Returns moe [n,d] (everything the experts add) and out = x + moe for the
     rows in ``tokens`` (all tokens when None).
     """
     x = np.asarray(x, dtype=np.float64)
@@ -218,18 +240,23 @@ def combine(x, idx, w, pos, expert_out, residual=True, tokens=None) -> dict:
         for r in range(k):
             if pos[t, r] >= 0:
                 moe[i] += w[t, r] * expert_out[(int(t), r)]
+    if shared_out is not None:
+        moe = moe + np.asarray(shared_out, dtype=np.float64)
     out = x[toks] + moe if residual else moe.copy()
     return dict(moe=moe, out=out)
 
 
 def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
             b_g=None, W_noise=None, eps=None, capacity_factor: Optional[float] = None,
-            C: Optional[int] = None, tokens=None, idx_override=None) -> dict:
+            C: Optional[int] = None, tokens=None, idx_override=None, shared: Optional[dict] = None) -> dict:
     """Forward pass of one sparse MoE layer, step by step.
 
     1 logits ([P4] s2) -> 2 top-k ([P4] s2) -> 3 gates ([P4] s2) ->
     4 capacity ([P5]) -> 5 dispatch ([P1] Lab 3) -> 6 experts on the kept
     assignments -> 7 combine + residual ([P4] s1, s3).
+    ``shared``: optional shared experts (keys W1s, W2s and optionally W3s,
+    b1s, b2s, as in ``shared_experts``), applied to every token and added in
+    the combine.
 
     ``tokens``: evaluate experts and combine only for these token ids
     (routing and dispatch always cover the whole batch, since capacity
@@ -262,8 +289,12 @@ def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
         y = expert(rows, e, act, W1, W3, W2, b1, b2)
         for i, p in enumerate(pairs):
             expert_out[p] = y[i]
-    comb = combine(x, idx, w, pos, expert_out, residual=True, tokens=toks)
-    return dict(H=H, idx=idx, w=w, C=C, tokens=toks, **disp, **comb)
+    sh = None
+    if shared is not None:
+        sh = shared_experts(x, act, shared["W1s"], shared["W2s"], shared.get("W3s"), shared.get("b1s"),
+                            shared.get("b2s"), tokens=toks)
+    comb = combine(x, idx, w, pos, expert_out, residual=True, tokens=toks, shared_out=sh)
+    return dict(H=H, idx=idx, w=w, C=C, tokens=toks, shared_out=sh, **disp, **comb)
 
 
 def near_ties(H: np.ndarray, k: int, thresh: float = 1e-4) -> dict:

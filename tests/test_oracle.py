@@ -435,3 +435,81 @@ def test_routing_stats_brute_force_and_token_order():
     for key in ("f", "P"):
         np.testing.assert_allclose(st2[key], st[key], atol=1e-15)
     assert st2["aux_loss"] == pytest.approx(st["aux_loss"], abs=1e-14)
+
+
+# ---------------------------------------------------------------- shared experts
+
+def _shared(seed, S=2, d=6, Fs=5, act=O.GELU, bias=True):
+    rng = np.random.default_rng(seed)
+    return dict(W1s=rng.normal(size=(S, Fs, d)) / math.sqrt(d), W3s=rng.normal(size=(S, Fs, d)) / math.sqrt(d),
+                W2s=rng.normal(size=(S, d, Fs)) / math.sqrt(Fs),
+                b1s=rng.normal(size=(S, Fs)) if (bias and act == O.GELU) else None,
+                b2s=rng.normal(size=(S, d)) if bias else None)
+
+
+def _torch_ffn(x, act, W1, W3, W2, b1, b2):
+    """One FFN in torch fp64 via F.linear (nn.Linear layout)."""
+    lin = torch.nn.functional.linear
+    t = lambda a: None if a is None else torch.tensor(a)
+    if act == O.GELU:
+        h = torch.nn.functional.gelu(lin(x, t(W1), t(b1)))
+    else:
+        h = torch.nn.functional.silu(lin(x, t(W1))) * lin(x, t(W3))
+    return lin(h, t(W2), t(b2))
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_shared_experts_alone_when_every_assignment_is_dropped(act):
+    """C = 0 drops every routed assignment: the layer is x + the shared experts'
+    sum, every token through every shared expert with weight 1 (torch fp64)."""
+    L = _tiny_layer(31, act=act)
+    S = _shared(32, act=act)
+    res = O.forward(L["x"], L["W_g"], 2, act, L["W1"], L["W2"], L["W3"], L["b1"], L["b2"], b_g=L["b_g"], C=0,
+                    shared=S)
+    assert res["dropped"] == 2 * L["x"].shape[0]
+    x = torch.tensor(L["x"])
+    want = sum(_torch_ffn(x, act, S["W1s"][s], S["W3s"][s], S["W2s"][s],
+                          None if S["b1s"] is None else S["b1s"][s], S["b2s"][s]) for s in range(2))
+    np.testing.assert_allclose(res["moe"], want.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["out"], (x + want).numpy(), rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_k_equals_E_with_shared_is_dense_mixture_plus_shared(act):
+    L = _tiny_layer(33, act=act)
+    S = _shared(34, S=1, act=act)
+    T, E = L["x"].shape[0], L["W_g"].shape[1]
+    res = O.forward(L["x"], L["W_g"], E, act, L["W1"], L["W2"], L["W3"], L["b1"], L["b2"], b_g=L["b_g"], C=T,
+                    shared=S)
+    x = torch.tensor(L["x"])
+    p = torch.softmax(x @ torch.tensor(L["W_g"]) + torch.tensor(L["b_g"]), dim=1)
+    moe = _torch_ffn(x, act, S["W1s"][0], S["W3s"][0], S["W2s"][0],
+                     None if S["b1s"] is None else S["b1s"][0], S["b2s"][0])
+    for e in range(E):
+        moe = moe + p[:, e:e + 1] * _torch_ffn(x, act, L["W1"][e], L["W3"][e], L["W2"][e],
+                                               None if L["b1"] is None else L["b1"][e], L["b2"][e])
+    np.testing.assert_allclose(res["moe"], moe.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_shared_expert_matches_elementwise_loops():
+    S = _shared(35, S=3, d=5, Fs=4, act=O.SWIGLU)
+    xr = np.random.default_rng(36).normal(size=(3, 5))
+    y = O.shared_experts(xr, O.SWIGLU, S["W1s"], S["W2s"], S["W3s"], None, S["b2s"])
+    for i in range(3):
+        want = sum(_loop_expert(xr[i], s, O.SWIGLU, S["W1s"], S["W3s"], S["W2s"], None, S["b2s"]) for s in range(3))
+        np.testing.assert_allclose(y[i], want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_shared_experts_equal_one_wide_ffn(act):
+    """S shared experts of width F_s are one FFN of width S*F_s: W1/W3 rows
+    stacked, W2 columns stacked, b1 concatenated, b2 summed (the form the
+    library takes them in)."""
+    S = _shared(37, S=3, d=6, Fs=4, act=act)
+    x = np.random.default_rng(38).normal(size=(9, 6))
+    wide = dict(W1s=S["W1s"].reshape(1, 12, 6), W3s=S["W3s"].reshape(1, 12, 6),
+                W2s=np.concatenate(list(S["W2s"]), axis=1)[None], b2s=S["b2s"].sum(axis=0)[None],
+                b1s=None if S["b1s"] is None else S["b1s"].reshape(1, 12))
+    a = O.shared_experts(x, act, S["W1s"], S["W2s"], S["W3s"], S["b1s"], S["b2s"])
+    b = O.shared_experts(x, act, wide["W1s"], wide["W2s"], wide["W3s"], wide["b1s"], wide["b2s"])
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
