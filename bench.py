@@ -216,7 +216,7 @@ def cpu_oracle_run(w, budget_s: float):
             return self.cache[e]
 
     # sub-batch size from the algorithmic work per token (fp64 BLAS ~1e11 flop/s)
-    per_tok = 2.0 * w.d * w.F * (3 if w.act == W.ACT_SWIGLU else 2) * w.k + 2.0 * w.d * w.E
+    per_tok = 2.0 * w.d * (3 if w.act == W.ACT_SWIGLU else 2) * (w.F * w.k + w.n_shared * w.F_shared) + 2.0 * w.d * w.E
     T_s = int(max(16, min(w.T, budget_s * 1e11 / per_tok / 2)))
     key = (w.name, T_s)
     if key not in _ORACLE_CACHE:
@@ -225,7 +225,9 @@ def cpu_oracle_run(w, budget_s: float):
         _ORACLE_CACHE[key] = (f(inp["x"]), f(inp["W_g"]), F64(inp["W1"]), F64(inp["W2"]), dict(
             W3=None if inp["W3"] is None else F64(inp["W3"]), b1=None if inp["b1"] is None else F64(inp["b1"]),
             b2=None if inp["b2"] is None else F64(inp["b2"]), b_g=f(inp["b_g"]), W_noise=f(inp["W_noise"]),
-            eps=f(inp["eps"]), capacity_factor=w.capacity_factor))
+            eps=f(inp["eps"]), capacity_factor=w.capacity_factor,
+            shared=None if inp["W1s"] is None else dict(
+                W1s=f(inp["W1s"]), W2s=f(inp["W2s"]), W3s=f(inp["W3s"]), b1s=f(inp["b1s"]), b2s=f(inp["b2s"]))))
     x, Wg, W1, W2, args = _ORACLE_CACHE[key]
     runs, tokens, t0 = 0, 0, time.perf_counter()
     while True:
@@ -277,6 +279,7 @@ def workload_config(w):
     return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
             "act": "swiglu" if w.act == W.ACT_SWIGLU else "gelu", "capacity_factor": w.capacity_factor,
             "noisy_gating": w.noisy, "dtype": w.dtype_name, "seed": w.seed,
+            **({"shared_experts": w.n_shared, "d_ff_shared_each": w.F_shared} if w.n_shared else {}),
             "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
 
 
@@ -305,7 +308,15 @@ def run_ours(a):
     g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
     C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
-    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act)
+    sw = W.shared_wide(g)
+    Fsh = 0 if sw["W1s"] is None else sw["W1s"].shape[0]
+    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act, d_ff_shared=Fsh)
+    shared_w = None
+    if Fsh:
+        b2s = None if sw["b2s_rows"] is None else sw["b2s_rows"].sum(dim=0).contiguous()
+        shared_t = dict(W1s=sw["W1s"], W2s=sw["W2s"], W3s=sw["W3s"], b1s=sw["b1s"], b2s=b2s)
+        shared_w = api.shared_weights(**shared_t)
+    shared_arg = ctypes.addressof(shared_w) if shared_w is not None else None
     ws = api.new_workspace(shape, C, dev)
     out = torch.empty(w.T, w.d, dtype=w.dtype, device=dev)
     counts = torch.empty(w.E, dtype=torch.int32, device=dev)
@@ -318,8 +329,8 @@ def run_ours(a):
         # the stream current at the call (the capture stream while a graph is recorded)
         sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
         return [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
-                P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), P(out),
-                None, None, None, None, P(counts), None, P(dropped), None, None, P(ws), ws.numel(), sptr]
+                P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), shared_arg,
+                P(out), None, None, None, None, P(counts), None, P(dropped), None, None, P(ws), ws.numel(), sptr]
 
     # the timed steps run as CUDA graphs of up to GRAPH_STEPS steps each (every
     # step the same C-ABI call, moe_forward_timed, its launches replayed
@@ -430,7 +441,8 @@ def run_ours(a):
 
     # ---------------- end to end through the public API with host buffers
     layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
-                         b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False)
+                         b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False,
+                         **(shared_t if Fsh else {}))
     x_host = inp["x"].pin_memory()
     eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
     out_host = torch.empty(w.T, w.d, dtype=w.dtype).pin_memory()
@@ -472,7 +484,7 @@ def run_ours(a):
     logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
     idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
     fa = fwd_args()
-    fa[15], fa[22] = P(idx_t), P(logits)
+    fa[16], fa[23] = P(idx_t), P(logits)
     _lib.check(lib.moe_forward(*fa), "moe_forward")
     st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
     sptr = ctypes.c_void_p(stream.cuda_stream)
@@ -503,6 +515,34 @@ def run_ours(a):
                      "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
                      "overflow": summ["overflow"]}
 
+    # ---------------- the shared experts alone (moe_shared_ffn: two dense GEMMs over
+    # every token), kernel time with L2 flushed before each call
+    shared_ffn = None
+    if Fsh:
+        y_sh = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+
+        def shared_call():
+            _lib.check(lib.moe_shared_ffn(ctypes.byref(shape), P(g["x"]), shared_arg, P(y_sh), P(ws), ws.numel(),
+                                          sptr), "moe_shared_ffn")
+
+        for _ in range(3):
+            shared_call()
+        hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_st)]
+        for i in range(n_st):
+            flush.zero_()
+            hev[i][0].record(stream)
+            shared_call()
+            hev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if api.get_device_error(ws) != 0:
+            raise RuntimeError("device-side error in moe_shared_ffn")
+        sh_ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in hev)
+        sh_flops = 2.0 * w.T * w.d * Fsh * ((2 if w.act == W.ACT_SWIGLU else 1) + 1)
+        shared_ffn = {"us_per_call": sh_ms * 1e3, "algorithmic_flops": sh_flops,
+                      "achieved_tflops": sh_flops / (sh_ms / 1e3) / 1e12,
+                      "frac_bf16": sh_flops / (sh_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                      "peak_source": peaks["source"] + " bf16 burst", "launches_per_call": 2}
+
     if rank != 0:
         if world > 1:
             dist.barrier()
@@ -522,9 +562,13 @@ def run_ours(a):
             "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic", "config": cfg,
             "stage_ms": {n: statistics.mean(v) for n, v in zip(
-                ["router_dispatch_gather", "expert_gemm1", "expert_gemm2_combine"], stage_ms)},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * a.steps,
+                ["shared_ffn_router_dispatch_gather" if Fsh else "router_dispatch_gather", "expert_gemm1",
+                 "expert_gemm2_combine"], stage_ms)},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": (KERNELS_PER_STEP + (2 if Fsh else 0)) * a.steps,
             "clocks": sampler.summary(), "routing_stats": routing_stats}
+    if shared_ffn is not None:
+        line["shared_ffn"] = shared_ffn
     print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -25,6 +25,8 @@
  *                         ("LLM part 09", s1 y = sum_i G(x)_i E_i(x); s3:
  *                         a dropped assignment bypasses its expert and the
  *                         residual carries the token)
+ *                         (+ the shared experts' output on every token, when
+ *                         the layer has shared experts; see moe_shared_t)
  *
  * Conventions for every entry point
  *   - All tensor arguments are DEVICE pointers of the current CUDA device,
@@ -78,7 +80,9 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
 
 /* Shape of one layer call.  T tokens of width d, E experts of hidden width
- * d_ff, top-k routing.  dtype is a moe_dtype_t, act a moe_act_t. */
+ * d_ff, top-k routing.  dtype is a moe_dtype_t, act a moe_act_t.
+ * d_ff_shared is the hidden width of the shared experts (0 = none; bf16
+ * needs a multiple of 64). */
 typedef struct {
   int64_t T;
   int32_t d;
@@ -87,7 +91,29 @@ typedef struct {
   int32_t d_ff;
   int32_t dtype;
   int32_t act;
+  int32_t d_ff_shared;
 } moe_shape_t;
+
+/* Shared experts ("Mixture-of-Experts Sparse Model Scaling", Advanced Theory
+ * & Extensions: dedicated shared experts that every token passes through
+ * unconditionally, next to the fine-grained routed ones; Real-World
+ * Applications: DeepSeek-MoE).  They have the routed experts' form (act of
+ * the shape) and enter the combine with weight 1.  S shared experts of width
+ * F_s are given as ONE FFN of width d_ff_shared = S*F_s: W1s and W3s stack
+ * the experts' rows, W2s stacks their columns, b1s concatenates, b2s is the
+ * sum of the experts' b2 (the same function, evaluated as one GEMM pair).
+ *   W1s [d_ff_shared,d] dtype           gate (SwiGLU) / up (GELU) projection
+ *   W3s [d_ff_shared,d] dtype | NULL    SwiGLU up projection (NULL for GELU)
+ *   W2s [d,d_ff_shared] dtype           down projection
+ *   b1s [d_ff_shared] fp32 | NULL       GELU only
+ *   b2s [d] fp32 | NULL */
+typedef struct {
+  const void* W1s;
+  const void* W3s;
+  const void* W2s;
+  const float* b1s;
+  const float* b2s;
+} moe_shared_t;
 
 /* Expert capacity C = ceil(capacity_factor * T * k / E), evaluated in double
  * in that order ("3D mixture-of-experts routing lab", Capacity card; the
@@ -192,21 +218,39 @@ MOE_API moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const v
                             const void* W2, const float* b1, const float* b2,
                             float* y_perm, void* ws, size_t ws_bytes, void* stream);
 
+/* The shared experts (see moe_shared_t) on every token: one dense FFN.
+ *   x         [T,d] dtype        tokens
+ *   shared    weights; required when shape->d_ff_shared > 0
+ *   y_shared  [T,d] fp32 out     the shared experts' summed output
+ *   ws, ws_bytes  a workspace of moe_workspace_size(shape, C) for any C
+ *                 (holds the [T,d_ff_shared] hidden activation)
+ * bf16: tcgen05 GEMMs with fp32 accumulation, the hidden activation rounded
+ * to bf16 between them, as for the routed experts.  shape->d_ff_shared == 0
+ * returns MOE_ERR_INVALID_ARG. */
+MOE_API moe_status_t moe_shared_ffn(const moe_shape_t* shape, const void* x, const moe_shared_t* shared,
+                                    float* y_shared, void* ws, size_t ws_bytes, void* stream);
+
 /* Step 5: weighted combine into the residual, one token at a time, ranks
- * summed in order 0..k-1 (deterministic).
+ * summed in order 0..k-1 (deterministic), then the shared experts' output.
  *   y_perm   [moe_max_rows,d] fp32   expert outputs (moe_expert_ffn)
  *   idx, w, pos [T,k], offsets [E+1]  as produced above
  *   residual [T,d] dtype | NULL       NULL = zero residual
+ *   y_shared [T,d] fp32 | NULL        shared experts' output (moe_shared_ffn),
+ *                                     added with weight 1; NULL = none
  *   out      [T,d] dtype out          residual + moe
- *   moe_out  [T,d] fp32 | NULL out    the weighted expert sum alone */
+ *   moe_out  [T,d] fp32 | NULL out    everything the experts add (routed
+ *                                     sum + shared output), alone */
 MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_perm,
                          const int32_t* idx, const float* w, const int32_t* pos,
-                         const int32_t* offsets, const void* residual, void* out,
-                         float* moe_out, void* stream);
+                         const int32_t* offsets, const void* residual, const float* y_shared,
+                         void* out, float* moe_out, void* stream);
 
 /* The whole layer: steps 1-5 on one stream, residual = x.
  *   capacity_factor  used when C_override < 0; else C = C_override
  *   x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2   as above
+ *   shared  moe_shared_t* | NULL: the shared experts' weights, required iff
+ *           shape->d_ff_shared > 0; their FFN runs first (on every token)
+ *           and its output is added in the combine
  *   out [T,d] dtype out; moe_out [T,d] fp32 | NULL out
  *   idx, w, pos [T,k], counts [E], offsets [E+1], dropped [1], stats [2]:
  *     optional outputs (NULL = keep them in the workspace only; stats as
@@ -219,14 +263,15 @@ MOE_API moe_status_t moe_forward(const moe_shape_t* shape, double capacity_facto
                          const void* x, const float* W_g, const float* b_g,
                          const float* W_noise, const float* eps, const void* W1,
                          const void* W3, const void* W2, const float* b1, const float* b2,
-                         void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
-                         int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
-                         float* logits, void* ws, size_t ws_bytes, void* stream);
+                         const moe_shared_t* shared, void* out, float* moe_out, int32_t* idx,
+                         float* w, int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
+                         int64_t* stats, float* logits, void* ws, size_t ws_bytes, void* stream);
 
 /* moe_forward, recording up to six CUDA events (cudaEvent_t, created by the
  * caller) on `stream` at the stage boundaries, so each stage can be timed
  * with cudaEventElapsedTime:
- *   stage_events[0] before the router        [1] after the router
+ *   stage_events[0] before the layer's first kernel (the shared experts'
+ *   FFN when there is one, else the router)  [1] after the router
  *   [2] after dispatch + gather              [3] after the first expert GEMM
  *   [4] after the second expert GEMM         [5] after the combine
  * A NULL entry records nothing at that boundary.  The layer's kernels are
@@ -239,9 +284,10 @@ MOE_API moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity
                                        const void* x, const float* W_g, const float* b_g,
                                        const float* W_noise, const float* eps, const void* W1,
                                        const void* W3, const void* W2, const float* b1, const float* b2,
-                                       void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
-                                       int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
-                                       float* logits, void* ws, size_t ws_bytes, void* stream,
+                                       const moe_shared_t* shared, void* out, float* moe_out, int32_t* idx,
+                                       float* w, int32_t* pos, int32_t* counts, int32_t* offsets,
+                                       int64_t* dropped, int64_t* stats, float* logits, void* ws,
+                                       size_t ws_bytes, void* stream,
                                        void* const* stage_events);
 
 /* Routing diagnostics of one batch and the auxiliary load-balancing loss

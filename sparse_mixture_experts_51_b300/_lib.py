@@ -20,7 +20,14 @@ MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
-                ("d_ff", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32)]
+                ("d_ff", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("d_ff_shared", ctypes.c_int32)]
+
+
+class MoeShared(ctypes.Structure):
+    """moe_shared_t: the shared experts' weights (device pointers)."""
+    _fields_ = [("W1s", ctypes.c_void_p), ("W3s", ctypes.c_void_p), ("W2s", ctypes.c_void_p),
+                ("b1s", ctypes.c_void_p), ("b2s", ctypes.c_void_p)]
 
 
 class MoeError(RuntimeError):
@@ -42,10 +49,11 @@ SIGNATURES = {
     "moe_dispatch_noalloc": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 10),
     "moe_expert_ffn": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                       ctypes.c_size_t, _P]),
-    "moe_combine": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "moe_forward": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 21
+    "moe_combine": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 10),
+    "moe_shared_ffn": (ctypes.c_int, [_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_forward": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 22
                     + [ctypes.c_size_t, _P]),
-    "moe_forward_timed": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 21
+    "moe_forward_timed": (ctypes.c_int, [_SHAPE, ctypes.c_double, ctypes.c_int32] + [_P] * 22
                           + [ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_routing_stats": (ctypes.c_int, [_SHAPE] + [_P] * 8 + [ctypes.c_size_t, _P]),
     "moe_get_device_error": (ctypes.c_int, [_P, _P]),

@@ -13,7 +13,7 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_BF16, MOE_F32, MoeError, MoeShape
+from ._lib import MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_BF16, MOE_F32, MoeError, MoeShape, MoeShared
 
 ACTS = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU, MOE_ACT_GELU: MOE_ACT_GELU, MOE_ACT_SWIGLU: MOE_ACT_SWIGLU}
 
@@ -41,9 +41,18 @@ def _stream(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def shape_of(T: int, d: int, E: int, k: int, d_ff: int, dtype: torch.dtype, act) -> MoeShape:
+def shape_of(T: int, d: int, E: int, k: int, d_ff: int, dtype: torch.dtype, act, d_ff_shared: int = 0) -> MoeShape:
     return MoeShape(T=int(T), d=int(d), E=int(E), k=int(k), d_ff=int(d_ff), dtype=_dtype_code(dtype),
-                    act=ACTS[act])
+                    act=ACTS[act], d_ff_shared=int(d_ff_shared))
+
+
+def shared_weights(W1s, W2s, W3s=None, b1s=None, b2s=None) -> MoeShared:
+    """moe_shared_t over device tensors (keep the tensors alive while it is used).
+    W1s, W3s [d_ff_shared, d]; W2s [d, d_ff_shared]; b1s [d_ff_shared]; b2s [d]."""
+    for t in (W1s, W2s, W3s, b1s, b2s):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("shared-expert weights must be contiguous")
+    return MoeShared(W1s=_ptr(W1s), W3s=_ptr(W3s), W2s=_ptr(W2s), b1s=_ptr(b1s), b2s=_ptr(b2s))
 
 
 def capacity(T: int, k: int, E: int, capacity_factor: float) -> int:
@@ -160,16 +169,34 @@ def expert_ffn(x_perm: torch.Tensor, offsets: torch.Tensor, W1: torch.Tensor, W2
     return y
 
 
+def shared_ffn(x: torch.Tensor, W1s: torch.Tensor, W2s: torch.Tensor, act, W3s=None, b1s=None, b2s=None,
+               ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The shared experts (one dense FFN of width d_ff_shared) on every token.
+    Returns y_shared fp32 [T, d]."""
+    T, d = x.shape
+    Fs = W1s.shape[0]
+    shape = shape_of(T, d, 1, 1, 64, x.dtype, act, d_ff_shared=Fs)
+    if ws is None:
+        ws = new_workspace(shape, 0, x.device)
+    y = torch.empty(T, d, dtype=torch.float32, device=x.device)
+    sh = shared_weights(W1s, W2s, W3s, b1s, b2s)
+    st = _lib.load().moe_shared_ffn(ctypes.byref(shape), _ptr(x), ctypes.addressof(sh), _ptr(y), _ptr(ws),
+                                    ws.numel(), _stream(stream))
+    _lib.check(st, "moe_shared_ffn")
+    return y
+
+
 def combine(y_perm, idx, w, pos, offsets, residual, E: int, C: int, out_dtype, d_ff: int = 64,
-            want_moe: bool = False, stream=None):
-    """out = residual + sum of kept w * y rows.  Returns (out, moe_out or None)."""
+            want_moe: bool = False, y_shared: Optional[torch.Tensor] = None, stream=None):
+    """out = residual + sum of kept w * y rows (+ y_shared).  Returns (out, moe_out or None)."""
     T, k = idx.shape
     d = y_perm.shape[1]
     shape = shape_of(T, d, E, k, d_ff, out_dtype, MOE_ACT_GELU)
     out = torch.empty(T, d, dtype=out_dtype, device=idx.device)
     moe = torch.empty(T, d, dtype=torch.float32, device=idx.device) if want_moe else None
     st = _lib.load().moe_combine(ctypes.byref(shape), int(C), _ptr(y_perm), _ptr(idx), _ptr(w), _ptr(pos),
-                                 _ptr(offsets), _ptr(residual), _ptr(out), _ptr(moe), _stream(stream))
+                                 _ptr(offsets), _ptr(residual), _ptr(y_shared), _ptr(out), _ptr(moe),
+                                 _stream(stream))
     _lib.check(st, "moe_combine")
     return out, moe
 
@@ -182,19 +209,26 @@ class MoELayer:
     routing outputs of the call (idx, w, pos, counts, offsets, dropped, and
     the router logits) when ``keep_routing`` is set, and
     ``layer.routing_stats()`` turns them into the routing diagnostics and the
-    auxiliary load-balancing loss.
+    auxiliary load-balancing loss.  ``W1s``/``W2s`` (and ``W3s``, ``b1s``,
+    ``b2s``) add shared experts: one dense FFN of width ``W1s.shape[0]`` that
+    every token passes through, added in the combine.
     """
 
     def __init__(self, W_g, W1, W2, k: int, act, W3=None, b_g=None, W_noise=None, b1=None, b2=None,
                  capacity_factor: Optional[float] = None, C: Optional[int] = None, keep_routing: bool = True,
-                 want_moe: bool = False):
+                 want_moe: bool = False, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None):
         if (capacity_factor is None) == (C is None):
             raise ValueError("give exactly one of capacity_factor and C")
+        if (W1s is None) != (W2s is None):
+            raise ValueError("shared experts need both W1s and W2s")
         self.W_g, self.W1, self.W2, self.W3 = W_g, W1, W2, W3
         self.b_g, self.W_noise, self.b1, self.b2 = b_g, W_noise, b1, b2
         self.k, self.act = int(k), ACTS[act]
         self.E, self.F, self.d = W1.shape
         self.dtype = W1.dtype
+        self.Fs = 0 if W1s is None else int(W1s.shape[0])
+        self._shared_t = (W1s, W2s, W3s, b1s, b2s)
+        self._shared = shared_weights(W1s, W2s, W3s, b1s, b2s) if W1s is not None else None
         self.capacity_factor, self.C_fixed = capacity_factor, C
         self.keep_routing, self.want_moe = keep_routing, want_moe
         self._ws = {}
@@ -220,7 +254,7 @@ class MoELayer:
         C = self.capacity(T)
         key = (T, C)
         if key not in self._ws:
-            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act)
+            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act, self.Fs)
             self._ws[key] = new_workspace(shape, C, self.W1.device)
         return self._ws[key]
 
@@ -228,7 +262,7 @@ class MoELayer:
                  stats: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         T = x.shape[0]
         C = self.capacity(T)
-        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act)
+        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act, self.Fs)
         ws = self.workspace(T)
         dev = x.device
         if out is None:
@@ -247,7 +281,9 @@ class MoELayer:
         st = _lib.load().moe_forward(
             ctypes.byref(shape), float(self.capacity_factor or 0.0), int(C if self.C_fixed is not None else -1),
             _ptr(x), _ptr(self.W_g), _ptr(self.b_g), _ptr(self.W_noise), _ptr(eps), _ptr(self.W1), _ptr(self.W3),
-            _ptr(self.W2), _ptr(self.b1), _ptr(self.b2), _ptr(out), _ptr(moe), g("idx"), g("w"), g("pos"),
+            _ptr(self.W2), _ptr(self.b1), _ptr(self.b2),
+            ctypes.addressof(self._shared) if self._shared is not None else None, _ptr(out), _ptr(moe),
+            g("idx"), g("w"), g("pos"),
             g("counts"), g("offsets"), g("dropped"), _ptr(stats), g("logits"), _ptr(ws), ws.numel(),
             _stream(stream))
         _lib.check(st, "moe_forward")
@@ -295,18 +331,19 @@ def _capture(layer, x, eps, out):
 
 def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=None, b1=None, b2=None,
             capacity_factor: Optional[float] = None, C: Optional[int] = None, want_moe: bool = False,
-            stats: Optional[torch.Tensor] = None, stream=None):
+            stats: Optional[torch.Tensor] = None, stream=None, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None):
     """One-shot whole-layer forward.  Returns (out, routing dict incl. 'moe' when want_moe)."""
     if C is None and capacity_factor is None:
         raise ValueError("give capacity_factor or C")
     if C is not None:
         capacity_factor = None
     layer = MoELayer(W_g, W1, W2, k, act, W3=W3, b_g=b_g, W_noise=W_noise, b1=b1, b2=b2,
-                     capacity_factor=capacity_factor, C=C, keep_routing=True, want_moe=want_moe)
+                     capacity_factor=capacity_factor, C=C, keep_routing=True, want_moe=want_moe,
+                     W1s=W1s, W2s=W2s, W3s=W3s, b1s=b1s, b2s=b2s)
     out = layer(x, eps=eps, stats=stats, stream=stream)
     return out, layer.last
 
 
 __all__ = ["capacity", "max_rows", "workspace_size", "new_workspace", "get_device_error", "route", "dispatch",
-           "expert_ffn", "combine", "forward", "routing_stats", "stats_summary", "STATS_SUMMARY", "MoELayer",
+           "expert_ffn", "shared_ffn", "shared_weights", "combine", "forward", "routing_stats", "stats_summary", "STATS_SUMMARY", "MoELayer",
            "CapturedForward", "MoeError", "shape_of"]

@@ -1,7 +1,8 @@
 // Weighted combine into the residual, and the fp32 CUDA-core expert FFN.
 //
 // Combine: out[t] = residual[t] + sum over kept ranks r (in order 0..k-1) of
-// w[t,r] * y_perm[offsets[idx[t,r]] + pos[t,r]]  ("LLM part 09: Sparse
+// w[t,r] * y_perm[offsets[idx[t,r]] + pos[t,r]], plus the shared experts'
+// output y_shared[t] when there is one  ("LLM part 09: Sparse
 // Mixture-of-Experts (MoE)", s1 output equation and s3 residual bypass of
 // dropped tokens; "Mixture-of-Experts Sparse Model Scaling", Lab 1 weighted
 // accumulation).  Each thread owns 8 consecutive elements of one token,
@@ -11,6 +12,7 @@
 // fp32 FFN: the grouped expert MLP on CUDA cores for fp32 layers (whose
 // tolerance rules out tf32/bf16 tensor cores): one warp per output element,
 // lanes split the reduction so every weight row is read with coalesced loads.
+// With no segment offsets it is one dense FFN over every row (shared experts).
 #include "common.cuh"
 #include "internal.h"
 
@@ -72,6 +74,12 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p, long long
       for (int i = 0; i < 4; ++i) rv[q + i] = r4[i];
     }
   }
+  float4 sv[V / 4];
+  if (p.y_shared) {
+    const float4* src = reinterpret_cast<const float4*>(p.y_shared + t * d + c);
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) sv[q] = __ldg(src + q);
+  }
   float acc[V];
 #pragma unroll
   for (int i = 0; i < V; ++i) acc[i] = 0.f;
@@ -104,6 +112,15 @@ __global__ void __launch_bounds__(256) combine_kernel(CombineParams p, long long
       acc[4 * q + 1] = fmaf(wt, yv[q].y, acc[4 * q + 1]);
       acc[4 * q + 2] = fmaf(wt, yv[q].z, acc[4 * q + 2]);
       acc[4 * q + 3] = fmaf(wt, yv[q].w, acc[4 * q + 3]);
+    }
+  }
+  if (p.y_shared) {
+#pragma unroll
+    for (int q = 0; q < V / 4; ++q) {
+      acc[4 * q] += sv[q].x;
+      acc[4 * q + 1] += sv[q].y;
+      acc[4 * q + 2] += sv[q].z;
+      acc[4 * q + 3] += sv[q].w;
     }
   }
   if (p.moe_out) {
@@ -152,6 +169,10 @@ __global__ void __launch_bounds__(256) combine_kernel4(CombineParams p) {
       acc[0] = fmaf(wt, q.x, acc[0]); acc[1] = fmaf(wt, q.y, acc[1]);
       acc[2] = fmaf(wt, q.z, acc[2]); acc[3] = fmaf(wt, q.w, acc[3]);
     }
+    if (p.y_shared) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p.y_shared + t * d + c));
+      acc[0] += q.x; acc[1] += q.y; acc[2] += q.z; acc[3] += q.w;
+    }
     if (p.moe_out) store4<float>(p.moe_out + t * d + c, acc);
     float o[4] = {acc[0], acc[1], acc[2], acc[3]};
     if (p.residual) {
@@ -182,8 +203,8 @@ __global__ void __launch_bounds__(256) ffn1_f32_kernel(FfnParams p) {
   const int f = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int32_t* off = p.offsets;
-  if (row >= off[p.E] || f >= p.F) return;
-  const int e = expert_of_row(off, p.E, row);
+  if (row >= (off ? off[p.E] : p.rows) || f >= p.F) return;
+  const int e = off ? expert_of_row(off, p.E, row) : 0;
   const float* xr = static_cast<const float*>(p.x_perm) + row * p.d;
   const float* w1 = static_cast<const float*>(p.W1) + (static_cast<long long>(e) * p.F + f) * p.d;
   float a = 0.f, u = 0.f;
@@ -210,8 +231,8 @@ __global__ void __launch_bounds__(256) ffn2_f32_kernel(FfnParams p) {
   const int i = blockIdx.y * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   const int32_t* off = p.offsets;
-  if (row >= off[p.E] || i >= p.d) return;
-  const int e = expert_of_row(off, p.E, row);
+  if (row >= (off ? off[p.E] : p.rows) || i >= p.d) return;
+  const int e = off ? expert_of_row(off, p.E, row) : 0;
   const float* hr = static_cast<const float*>(p.h) + row * p.F;
   const float* w2 = static_cast<const float*>(p.W2) + (static_cast<long long>(e) * p.d + i) * p.F;
   float a = 0.f;

@@ -1,7 +1,8 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
 // Each expert e owns the rows [offsets[e], offsets[e+1]) of the expert-grouped
-// activations and computes, in nn.Linear layout (K contiguous for A and B):
+// activations (a dense FFN, such as the shared experts, is one group holding
+// every row) and computes, in nn.Linear layout (K contiguous for A and B):
 //   GELU   : h = gelu(A W1[e]^T + b1[e])                 -> bf16 [rows, F]
 //   SwiGLU : h = silu(A W1[e]^T) * (A W3[e]^T)           -> bf16 [rows, F]
 //   down   : y = h W2[e]^T + b2[e]                       -> fp32 [rows, d]
@@ -61,7 +62,8 @@ struct Cfg {
 enum { MODE_GELU = 0, MODE_SWIGLU = 1, MODE_DOWN = 2 };
 
 struct GemmArgs {
-  const int32_t* offsets;
+  const int32_t* offsets;  // [E+1] segment starts; null: one dense group of dense_rows rows
+  int dense_rows;
   int E;
   int N_out;      // output columns
   int N_w;        // weight rows per expert in the B tensor
@@ -143,9 +145,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // the prologue above overlaps the predecessor's tail; its outputs (the
   // grouped rows and their segment offsets) are read only from here on
   pdl_wait();
+  auto seg = [&](int e) -> int { return g.offsets ? g.offsets[e] : (e == 0 ? 0 : g.dense_rows); };
   // ---- per-expert tile counts from the segment offsets
   for (int e = tid; e < E; e += NTHREADS) {
-    const int cnt = g.offsets[e + 1] - g.offsets[e];
+    const int cnt = seg(e + 1) - seg(e);
     s_mt[e] = cnt > 0 ? (cnt + C::TILE_M - 1) / C::TILE_M : 0;
   }
   __syncthreads();
@@ -170,8 +173,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int local = tile - s_tstart[ecur];
     const int mt = s_mt[ecur];
     const int nb = local / mt, mb = local - nb * mt;
-    const int seg0 = g.offsets[ecur];
-    const int cnt = g.offsets[ecur + 1] - seg0;
+    const int seg0 = seg(ecur);
+    const int cnt = seg(ecur + 1) - seg0;
     ti.e = ecur;
     ti.row0 = seg0 + mb * C::TILE_M;
     ti.rows_valid = min(C::TILE_M, cnt - mb * C::TILE_M);
@@ -425,6 +428,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
 
   GemmArgs g1{};
   g1.offsets = p.offsets;
+  g1.dense_rows = p.offsets ? 0 : static_cast<int>(p.rows);
   g1.E = p.E;
   g1.N_out = p.F;
   g1.N_w = p.F;
@@ -451,6 +455,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
 
   GemmArgs g2{};
   g2.offsets = p.offsets;
+  g2.dense_rows = g1.dense_rows;
   g2.E = p.E;
   g2.N_out = p.d;
   g2.N_w = p.d;

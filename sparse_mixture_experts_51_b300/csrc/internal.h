@@ -52,6 +52,8 @@ struct WsLayout {
   size_t stats_ticket;  // int32 last-block ticket of moe_routing_stats (self-resetting)
   size_t stats_part;    // fp64 [kStatsMaxBlocks][E+1] per-block sums of p (and entropy)
   size_t stats_load;    // int32 [kStatsMaxBlocks][E] per-block routed loads
+  size_t h_shared;      // [T,d_ff_shared] dtype: hidden activation of the shared experts
+  size_t y_shared;      // [T,d] fp32: shared experts' output
   size_t idx, w, pos;        // [T,k] int32 / fp32 / int32
   size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
   size_t counts, offsets;    // [E], [E+1] int32
@@ -131,7 +133,7 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t st);
 
 struct FfnParams {
   const void* x_perm;
-  const int32_t* offsets;
+  const int32_t* offsets;  // [E+1]; null: a dense FFN (E = 1) over all `rows` rows
   const void* W1;
   const void* W3;
   const void* W2;
@@ -149,6 +151,7 @@ cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st);
 
 struct CombineParams {
   const float* y_perm;
+  const float* y_shared;  // [T,d] fp32 or null: shared experts' output, added after the ranks
   const int32_t* row_of;  // [T,k] grouped rows (-1 dropped); when set, idx/pos/offsets are not read
   const int32_t* idx;
   const float* w;

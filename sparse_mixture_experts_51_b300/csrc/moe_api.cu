@@ -39,6 +39,9 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.stats_ticket = take(sizeof(int));
   L.stats_part = take(sizeof(double) * static_cast<size_t>(kStatsMaxBlocks) * (s.E + 1));
   L.stats_load = take(sizeof(int) * static_cast<size_t>(kStatsMaxBlocks) * s.E);
+  // (the regions up to here do not depend on C: any C's workspace holds them)
+  L.h_shared = take(b * static_cast<size_t>(s.T) * s.d_ff_shared);
+  L.y_shared = take(s.d_ff_shared > 0 ? sizeof(float) * static_cast<size_t>(s.T) * s.d : 0);
   L.idx = take(sizeof(int32_t) * Tk);
   L.w = take(sizeof(float) * Tk);
   L.pos = take(sizeof(int32_t) * Tk);
@@ -65,6 +68,8 @@ moe_status_t check_shape(const moe_shape_t* s) {
   if (s->E > kMaxExperts || s->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   if (s->dtype == MOE_BF16 && (s->d % 64 != 0 || s->d_ff % 64 != 0)) return MOE_ERR_UNSUPPORTED;
   if (s->dtype == MOE_F32 && s->d % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->d_ff_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (s->dtype == MOE_BF16 && s->d_ff_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -240,6 +245,50 @@ static moe_status_t check_experts(const moe_shape_t* shape, const void* W1, cons
   return MOE_OK;
 }
 
+static moe_status_t check_shared(const moe_shape_t* shape, const moe_shared_t* sh) {
+  if (shape->d_ff_shared == 0) return sh == nullptr ? MOE_OK : MOE_ERR_INVALID_ARG;
+  if (sh == nullptr || sh->W1s == nullptr || sh->W2s == nullptr) return MOE_ERR_INVALID_ARG;
+  if (shape->act == MOE_ACT_SWIGLU && (sh->W3s == nullptr || sh->b1s != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->act == MOE_ACT_GELU && sh->W3s != nullptr) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(sh->W1s) || !aligned16(sh->W2s) || (sh->W3s && !aligned16(sh->W3s))) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// the shared experts as one dense FFN over every token (no offsets: one group of T rows)
+static moe_status_t shared_impl(const moe_shape_t* shape, const void* x, const moe_shared_t* sh, float* y_shared,
+                                void* ws, const WsLayout& L, cudaStream_t st) {
+  if (shape->T == 0) return MOE_OK;
+  FfnParams fp{};
+  fp.x_perm = x;
+  fp.offsets = nullptr;
+  fp.W1 = sh->W1s;
+  fp.W3 = sh->W3s;
+  fp.W2 = sh->W2s;
+  fp.b1 = sh->b1s;
+  fp.b2 = sh->b2s;
+  fp.h = at<void>(ws, L.h_shared);
+  fp.y_perm = y_shared;
+  fp.E = 1;
+  fp.d = shape->d;
+  fp.F = shape->d_ff_shared;
+  fp.act = shape->act;
+  fp.rows = shape->T;
+  fp.err = at<int>(ws, L.err);
+  return cuda_status(shape->dtype == MOE_BF16 ? launch_ffn_bf16(fp, st) : launch_ffn_f32(fp, st));
+}
+
+moe_status_t moe_shared_ffn(const moe_shape_t* shape, const void* x, const moe_shared_t* shared, float* y_shared,
+                            void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->d_ff_shared == 0) return MOE_ERR_INVALID_ARG;
+  if ((st = check_shared(shape, shared)) != MOE_OK) return st;
+  if (shape->T > 0 && (x == nullptr || y_shared == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && (!aligned16(x) || !aligned16(y_shared))) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(shape, 0, ws, ws_bytes)) != MOE_OK) return st;
+  return shared_impl(shape, x, shared, y_shared, ws, ws_layout(*shape, 0), static_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const void* x_perm, const int32_t* offsets,
                             const void* W1, const void* W3, const void* W2, const float* b1, const float* b2,
                             float* y_perm, void* ws, size_t ws_bytes, void* stream) {
@@ -256,10 +305,11 @@ moe_status_t moe_expert_ffn(const moe_shape_t* shape, int32_t C, const void* x_p
 
 static moe_status_t combine_impl(const moe_shape_t* shape, long long rows, const float* y_perm, const int32_t* idx,
                                  const float* w, const int32_t* pos, const int32_t* offsets, const void* residual,
-                                 void* out, float* moe_out, int* err, cudaStream_t st,
+                                 const float* y_shared, void* out, float* moe_out, int* err, cudaStream_t st,
                                  const int32_t* row_of = nullptr) {
   CombineParams cp{};
   cp.y_perm = y_perm;
+  cp.y_shared = y_shared;
   cp.row_of = row_of;
   cp.idx = idx;
   cp.w = w;
@@ -279,8 +329,8 @@ static moe_status_t combine_impl(const moe_shape_t* shape, long long rows, const
 }
 
 moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_perm, const int32_t* idx,
-                         const float* w, const int32_t* pos, const int32_t* offsets, const void* residual, void* out,
-                         float* moe_out, void* stream) {
+                         const float* w, const int32_t* pos, const int32_t* offsets, const void* residual,
+                         const float* y_shared, void* out, float* moe_out, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (C < 0) return MOE_ERR_INVALID_ARG;
@@ -289,16 +339,17 @@ moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_per
   const WsLayout L = ws_layout(*shape, C);
   if (L.rows > 0 && y_perm == nullptr) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (!aligned16(out) || (residual && !aligned16(residual)) || (moe_out && !aligned16(moe_out)) ||
-                       (y_perm && !aligned16(y_perm))))
+                       (y_perm && !aligned16(y_perm)) || (y_shared && !aligned16(y_shared))))
     return MOE_ERR_UNSUPPORTED;
-  return combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, residual, out, moe_out, nullptr,
+  return combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, residual, y_shared, out, moe_out, nullptr,
                       static_cast<cudaStream_t>(stream));
 }
 
 static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_factor, int32_t C_override,
                                  const void* x, const float* W_g, const float* b_g, const float* W_noise,
                                  const float* eps, const void* W1, const void* W3, const void* W2, const float* b1,
-                                 const float* b2, void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos,
+                                 const float* b2, const moe_shared_t* shared, void* out, float* moe_out,
+                                 int32_t* idx, float* w, int32_t* pos,
                                  int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
                                  float* logits, void* ws, size_t ws_bytes, void* stream,
                                  void* const* stage_events) {
@@ -313,6 +364,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   if ((W_noise == nullptr) != (eps == nullptr)) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (x == nullptr || out == nullptr)) return MOE_ERR_INVALID_ARG;
   if ((st = check_experts(shape, W1, W3, W2, b1)) != MOE_OK) return st;
+  if ((st = check_shared(shape, shared)) != MOE_OK) return st;
   if (shape->T > 0 && (!aligned16(x) || !aligned16(out) || (moe_out && !aligned16(moe_out))))
     return MOE_ERR_UNSUPPORTED;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
@@ -339,6 +391,12 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   if (dropped == nullptr) dropped = at<int64_t>(ws, L.dropped);
 
   if ((st = mark(0)) != MOE_OK) return st;
+  // the shared experts need no routing: their FFN runs first
+  float* y_sh = nullptr;
+  if (shape->d_ff_shared > 0) {
+    y_sh = at<float>(ws, L.y_shared);
+    if ((st = shared_impl(shape, x, shared, y_sh, ws, L, s)) != MOE_OK) return st;
+  }
   if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, stream)) != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   int32_t* row_of = at<int32_t>(ws, L.row_of);
@@ -371,7 +429,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     if ((st = mark(3)) != MOE_OK) return st;
   }
   if ((st = mark(4)) != MOE_OK) return st;
-  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, out, moe_out, at<int>(ws, L.err), s,
+  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, y_sh, out, moe_out, at<int>(ws, L.err), s,
                         row_of)) != MOE_OK)
     return st;
   return mark(5);
@@ -379,21 +437,22 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
 
 moe_status_t moe_forward(const moe_shape_t* shape, double capacity_factor, int32_t C_override, const void* x,
                          const float* W_g, const float* b_g, const float* W_noise, const float* eps, const void* W1,
-                         const void* W3, const void* W2, const float* b1, const float* b2, void* out, float* moe_out,
-                         int32_t* idx, float* w, int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
-                         int64_t* stats, float* logits, void* ws, size_t ws_bytes, void* stream) {
-  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
+                         const void* W3, const void* W2, const float* b1, const float* b2, const moe_shared_t* shared,
+                         void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos, int32_t* counts,
+                         int32_t* offsets, int64_t* dropped, int64_t* stats, float* logits, void* ws, size_t ws_bytes,
+                         void* stream) {
+  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, shared, out,
                       moe_out, idx, w, pos, counts, offsets, dropped, stats, logits, ws, ws_bytes, stream, nullptr);
 }
 
 moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity_factor, int32_t C_override, const void* x,
                                const float* W_g, const float* b_g, const float* W_noise, const float* eps,
                                const void* W1, const void* W3, const void* W2, const float* b1, const float* b2,
-                               void* out, float* moe_out, int32_t* idx, float* w, int32_t* pos, int32_t* counts,
-                               int32_t* offsets, int64_t* dropped, int64_t* stats, float* logits, void* ws,
-                               size_t ws_bytes, void* stream, void* const* stage_events) {
+                               const moe_shared_t* shared, void* out, float* moe_out, int32_t* idx, float* w,
+                               int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped, int64_t* stats,
+                               float* logits, void* ws, size_t ws_bytes, void* stream, void* const* stage_events) {
   if (stage_events == nullptr) return MOE_ERR_INVALID_ARG;
-  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, out,
+  return forward_impl(shape, capacity_factor, C_override, x, W_g, b_g, W_noise, eps, W1, W3, W2, b1, b2, shared, out,
                       moe_out, idx, w, pos, counts, offsets, dropped, stats, logits, ws, ws_bytes, stream,
                       stage_events);
 }

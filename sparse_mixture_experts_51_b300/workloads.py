@@ -13,14 +13,18 @@ Shapes follow the five layer configurations this library is measured on:
   switch_top1     T=32768 d=768  E=64 k=1 GELU   F=3072  cf=1.0   bf16,
                   Zipf router bias and noisy gating
   decode_t128     T=128   d=2048 E=64 k=6 SwiGLU F=1408  cf=2.0   bf16
+and one layer with shared experts (the next-step extension):
+  shared_t4096    T=4096  d=2048 E=64 k=6 SwiGLU F=1408  cf=1.25  bf16,
+                  plus 2 shared experts of width 1408
 
 Value recipe (all draws fp32 standard normal from one CPU torch.Generator
 seeded per workload, scaled, then cast to the storage dtype):
   x ~ N(0,1); W_g ~ N(0, 1/d); W1, W3 ~ N(0, 1/d); W2 ~ N(0, 1/F)
   (tiny_fp32 takes "N(0, 1/d)" literally for every weight, W2 included);
   biases zero (tiny_fp32 carries explicit zero b1/b2; the others have none);
-  switch_top1: b_g[e] = 2*ln(1/(e+1)), W_noise ~ N(0, 1/d), eps ~ N(0,1)[T,E].
-The draw order is fixed: x, W_g, W_noise, eps, W1, W3, W2.
+  switch_top1: b_g[e] = 2*ln(1/(e+1)), W_noise ~ N(0, 1/d), eps ~ N(0,1)[T,E];
+  shared experts: W1s, W3s ~ N(0, 1/d) [S,F_s,d]; W2s ~ N(0, 1/F_s) [S,d,F_s].
+The draw order is fixed: x, W_g, W_noise, eps, W1, W3, W2, W1s, W3s, W2s.
 
 Layouts (row-major, nn.Linear style, K contiguous):
   x [T,d]; W_g [d,E] fp32; b_g [E] fp32; W_noise [d,E] fp32; eps [T,E] fp32;
@@ -54,6 +58,8 @@ class Workload:
     zipf_bias: bool = False  # router bias b_e = 2 ln(1/(e+1))
     expert_bias: bool = False  # explicit (zero) b1/b2 tensors
     weight_std_literal_d: bool = False  # every weight ~N(0,1/d)
+    n_shared: int = 0        # shared experts (every token, weight 1)
+    F_shared: int = 0        # hidden width of each shared expert
 
     @property
     def dtype_name(self) -> str:
@@ -83,6 +89,10 @@ WORKLOADS = {
                             noisy=True, zipf_bias=True),
     "decode_t128": Workload("decode_t128", T=128, d=2048, E=64, k=6, F=1408, act=ACT_SWIGLU,
                             capacity_factor=2.0, dtype=torch.bfloat16, seed=5),
+    # fine-grained routed experts plus two always-on shared experts of the
+    # same width (the DeepSeek-MoE layout, at a prefill-sized batch)
+    "shared_t4096": Workload("shared_t4096", T=4096, d=2048, E=64, k=6, F=1408, act=ACT_SWIGLU,
+                             capacity_factor=1.25, dtype=torch.bfloat16, seed=6, n_shared=2, F_shared=1408),
 }
 ORDER = ["tiny_fp32", "bf16_t4096", "mixtral_t16384", "switch_top1", "decode_t128"]
 
@@ -124,8 +134,34 @@ def make_inputs(w: Workload) -> dict:
     cast = (lambda t: t) if w.dtype == torch.float32 else (lambda t: t.to(w.dtype))
     out = dict(x=cast(x), W_g=W_g, b_g=b_g, W_noise=W_noise, eps=eps,
                W1=cast(W1), W3=None if W3 is None else cast(W3), W2=cast(W2),
-               b1=b1, b2=b2)
+               b1=b1, b2=b2, W1s=None, W3s=None, W2s=None, b1s=None, b2s=None)
+    if w.n_shared > 0:
+        # drawn after every routed tensor, so the routed inputs do not depend on them
+        S, Fs = w.n_shared, w.F_shared
+        out["W1s"] = cast(_normal(g, (S, Fs, d), std_d))
+        out["W3s"] = cast(_normal(g, (S, Fs, d), std_d)) if w.act == ACT_SWIGLU else None
+        out["W2s"] = cast(_normal(g, (S, d, Fs), 1.0 / math.sqrt(Fs)))
+        if w.expert_bias:
+            out["b1s"] = torch.zeros(S, Fs, dtype=torch.float32) if w.act == ACT_GELU else None
+            out["b2s"] = torch.zeros(S, d, dtype=torch.float32)
     return out
+
+
+def shared_wide(inp: dict) -> dict:
+    """The shared experts of ``inp`` (per expert: W1s, W3s [S,F_s,d], W2s
+    [S,d,F_s], b1s [S,F_s], b2s [S,d]) laid out as the one FFN of width S*F_s
+    that the library takes: W1s/W3s rows stacked, W2s columns stacked, b1s
+    concatenated; b2s becomes the list of per-expert rows to be summed by the
+    caller (returned stacked as [S,d]).  Pure layout: no arithmetic."""
+    if inp.get("W1s") is None:
+        return dict(W1s=None, W3s=None, W2s=None, b1s=None, b2s_rows=None)
+    W1s, W3s, W2s = inp["W1s"], inp["W3s"], inp["W2s"]
+    S, Fs, d = W1s.shape
+    return dict(W1s=W1s.reshape(S * Fs, d).contiguous(),
+                W3s=None if W3s is None else W3s.reshape(S * Fs, d).contiguous(),
+                W2s=torch.cat(list(W2s), dim=1).contiguous(),
+                b1s=None if inp.get("b1s") is None else inp["b1s"].reshape(S * Fs).contiguous(),
+                b2s_rows=inp.get("b2s"))
 
 
 def make_tokens(w: Workload, seed: int) -> tuple:

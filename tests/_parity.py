@@ -33,18 +33,38 @@ def to_gpu(inp: dict, dev="cuda") -> dict:
     return {k: (None if v is None else v.to(dev).contiguous()) for k, v in inp.items()}
 
 
+def shared_args(g: dict) -> dict:
+    """The library's form of the shared experts in ``g`` (one FFN of width
+    S*F_s; b2 of the wide FFN = the sum of the experts' b2), or no shared
+    experts."""
+    sw = W.shared_wide(g)
+    if sw["W1s"] is None:
+        return {}
+    b2 = None if sw["b2s_rows"] is None else sw["b2s_rows"].sum(dim=0).contiguous()
+    return dict(W1s=sw["W1s"], W2s=sw["W2s"], W3s=sw["W3s"], b1s=sw["b1s"], b2s=b2)
+
+
 def gpu_forward(w: W.Workload, g: dict, C=None, want_moe=True):
     stats = torch.zeros(2, dtype=torch.int64, device="cuda")
     act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
     out, r = api.forward(g["x"], g["W_g"], w.k, act, g["W1"], g["W2"], W3=g["W3"], b_g=g["b_g"],
                          W_noise=g["W_noise"], eps=g["eps"], b1=g["b1"], b2=g["b2"],
                          capacity_factor=None if C is not None else w.capacity_factor, C=C,
-                         want_moe=want_moe, stats=stats)
+                         want_moe=want_moe, stats=stats, **shared_args(g))
     torch.cuda.synchronize()
     res = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in r.items()}
     res["out"] = out.cpu()
     res["stats"] = stats.cpu()
     return res
+
+
+def oracle_shared(inp: dict):
+    """The shared experts of ``inp`` per expert, widened to fp64, or None."""
+    if inp.get("W1s") is None:
+        return None
+    f = W.as_f64_numpy
+    return dict(W1s=f(inp["W1s"]), W2s=f(inp["W2s"]), W3s=f(inp["W3s"]), b1s=f(inp.get("b1s")),
+                b2s=f(inp.get("b2s")))
 
 
 def oracle_forward(w: W.Workload, inp: dict, C=None, tokens=None, idx_override=None):
@@ -55,7 +75,7 @@ def oracle_forward(w: W.Workload, inp: dict, C=None, tokens=None, idx_override=N
                      b2=None if inp["b2"] is None else F64Experts(inp["b2"]),
                      b_g=f(inp["b_g"]), W_noise=f(inp["W_noise"]), eps=f(inp["eps"]),
                      capacity_factor=w.capacity_factor if C is None else None, C=C, tokens=tokens,
-                     idx_override=idx_override)
+                     idx_override=idx_override, shared=oracle_shared(inp))
 
 
 def tolerance(w: W.Workload) -> float:

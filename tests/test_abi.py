@@ -125,8 +125,8 @@ def test_dispatch_ffn_combine_argument_errors(lib):
     assert lib.moe_expert_ffn(ctypes.byref(sg), 40, f, f, f, f, f, f, None, f, f, n, None) == INVALID
     assert lib.moe_expert_ffn(ctypes.byref(s), 40, f, f, P(FAKE + 8), None, f, None, None, f, f, n, None) == UNSUPPORTED
     # combine: missing pieces
-    assert lib.moe_combine(ctypes.byref(s), 40, f, None, f, f, f, None, f, None, None) == INVALID
-    assert lib.moe_combine(ctypes.byref(s), 40, None, f, f, f, f, None, f, None, None) == INVALID
+    assert lib.moe_combine(ctypes.byref(s), 40, f, None, f, f, f, None, None, f, None, None) == INVALID
+    assert lib.moe_combine(ctypes.byref(s), 40, None, f, f, f, f, None, None, f, None, None) == INVALID
 
 
 @no_gpu
@@ -134,7 +134,8 @@ def test_forward_argument_errors(lib):
     s = _shape()
     f = P(FAKE)
     st, n = _ws(lib, s, 40)
-    args = [f, f, None, None, None, f, None, f, None, None, f, None, None, None, None, None, None, None, None, None]
+    args = [f, f, None, None, None, f, None, f, None, None, None, f, None, None, None, None, None, None, None, None,
+            None]
     # bad capacity factor with no override
     assert lib.moe_forward(ctypes.byref(s), 0.0, -1, *args, f, n, None) == INVALID
     # a workspace sized for C=10 (40 grouped rows) is too small for cf=1.25 (C=40, 128 rows)
@@ -144,7 +145,7 @@ def test_forward_argument_errors(lib):
     assert lib.moe_forward(ctypes.byref(s), 1.0, 40, *args, f, n10, None) == WORKSPACE
     # missing output
     bad = list(args)
-    bad[10] = None
+    bad[11] = None
     assert lib.moe_forward(ctypes.byref(s), 1.25, -1, *bad, f, n, None) == INVALID
 
 
@@ -170,3 +171,37 @@ def test_routing_stats_argument_errors(lib):
     assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, None, n, None) == WORKSPACE
     assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, P(FAKE + 16), n, None) == WORKSPACE
     assert lib.moe_routing_stats(ctypes.byref(s), f, f, f, f, f, f, f, f, n - 256, None) == WORKSPACE
+
+
+@no_gpu
+def test_shared_expert_argument_errors(lib):
+    from sparse_mixture_experts_51_b300._lib import MoeShared
+    f = P(FAKE)
+    s0 = _shape()                      # no shared experts
+    s = _shape(d_ff_shared=128)        # GELU layer with a shared FFN of width 128
+    sg = _shape(act=1, d_ff_shared=128)
+    st, n = _ws(lib, s, 0)
+    assert st == OK and n > _ws(lib, s0, 0)[1]  # the shared activations live in the workspace
+    gelu_w = MoeShared(W1s=FAKE, W3s=None, W2s=FAKE, b1s=None, b2s=None)
+    swiglu_no_w3 = MoeShared(W1s=FAKE, W3s=None, W2s=FAKE, b1s=None, b2s=None)
+    gelu_with_w3 = MoeShared(W1s=FAKE, W3s=FAKE, W2s=FAKE, b1s=None, b2s=None)
+    addr = ctypes.addressof
+    # moe_shared_ffn: no shared width, missing weights, wrong W3 / b1 for the activation
+    assert lib.moe_shared_ffn(ctypes.byref(s0), f, addr(gelu_w), f, f, n, None) == INVALID
+    assert lib.moe_shared_ffn(ctypes.byref(s), f, None, f, f, n, None) == INVALID
+    assert lib.moe_shared_ffn(ctypes.byref(sg), f, addr(swiglu_no_w3), f, f, n, None) == INVALID
+    assert lib.moe_shared_ffn(ctypes.byref(s), f, addr(gelu_with_w3), f, f, n, None) == INVALID
+    assert lib.moe_shared_ffn(ctypes.byref(s), f, addr(gelu_w), None, f, n, None) == INVALID
+    # a workspace sized without the shared activations is too small
+    assert lib.moe_shared_ffn(ctypes.byref(s), f, addr(gelu_w), f, f, _ws(lib, s0, 0)[1], None) == WORKSPACE
+    # shape checks: negative or (bf16) non-multiple-of-64 shared width
+    assert _ws(lib, _shape(d_ff_shared=-64), 40)[0] == INVALID
+    assert _ws(lib, _shape(d_ff_shared=100), 40)[0] == UNSUPPORTED
+    # moe_forward: shared weights required iff d_ff_shared > 0
+    st, nf = _ws(lib, s, 40)
+    args = [f, f, None, None, None, f, None, f, None, None, None, f, None, None, None, None, None, None, None, None,
+            None]
+    assert lib.moe_forward(ctypes.byref(s), 1.25, -1, *args, f, nf, None) == INVALID
+    bad = list(args)
+    bad[10] = addr(gelu_w)
+    assert lib.moe_forward(ctypes.byref(s0), 1.25, -1, *bad, f, nf, None) == INVALID
