@@ -151,6 +151,46 @@ def dispatch(idx: np.ndarray, E: int, C: int) -> dict:
     return dict(pos=pos, load=load, counts=counts, offsets=offsets, dropped=int(dropped))
 
 
+def softmax_rows(H: np.ndarray) -> np.ndarray:
+    """Router probabilities p[t,e] = softmax over all E experts of H[t]
+    ([P2] Level 2: a softmax turns the router scores into weights)."""
+    H = np.asarray(H, dtype=np.float64)
+    z = np.exp(H - H.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def expert_choice(H: np.ndarray, C: int) -> dict:
+    """Expert-choice routing ([P1] "Advanced Theory & Extensions": each expert
+    selects from the batch the top tokens it wants, up to its capacity, so
+    every expert is filled; a token may be taken by no expert or by several).
+
+    Readings: expert e ranks the tokens by its router score H[t,e] (the
+    logit: [P2] Level 2 calls the router's per-expert outputs scores) and
+    takes the min(C, T) highest, equal scores going to the lower token index;
+    the gate of a chosen (t, e) is the router probability p[t,e] (softmax
+    over all E experts), not renormalised over the experts that chose t.
+
+    Returns sel int64 [E, C'] (chosen tokens of each expert, ascending),
+    gates [E, C'] (p of those pairs), chosen bool [T,E], counts [E] (= C'),
+    dropped (tokens no expert chose).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    T, E = H.shape
+    Cp = min(int(C), T)
+    P = softmax_rows(H)
+    sel = np.zeros((E, Cp), dtype=np.int64)
+    chosen = np.zeros((T, E), dtype=bool)
+    for e in range(E):
+        # a stable sort of -H keeps lower token indices first among equal scores
+        top = np.sort(np.argsort(-H[:, e], kind="stable")[:Cp])
+        sel[e] = top
+        chosen[top, e] = True
+    gates = np.array([[P[t, e] for t in sel[e]] for e in range(E)], dtype=np.float64).reshape(E, Cp)
+    counts = np.full(E, Cp, dtype=np.int64)
+    dropped = int(T - np.count_nonzero(chosen.any(axis=1)))
+    return dict(sel=sel, gates=gates, chosen=chosen, counts=counts, dropped=dropped, P=P)
+
+
 # --------------------------------------------------------------------------
 # experts
 # --------------------------------------------------------------------------
@@ -295,6 +335,49 @@ def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
                             shared.get("b2s"), tokens=toks)
     comb = combine(x, idx, w, pos, expert_out, residual=True, tokens=toks, shared_out=sh)
     return dict(H=H, idx=idx, w=w, C=C, tokens=toks, shared_out=sh, **disp, **comb)
+
+
+def forward_expert_choice(x, W_g, act: int, W1, W2, W3=None, b1=None, b2=None, b_g=None, W_noise=None, eps=None,
+                          C: Optional[int] = None, capacity_factor: Optional[float] = None, k: int = 1,
+                          tokens=None, shared: Optional[dict] = None) -> dict:
+    """Forward pass of one MoE layer with expert-choice routing ([P1]
+    "Advanced Theory & Extensions").
+
+    1 logits ([P4] s2) -> 2 each expert's top-C tokens (``expert_choice``)
+    -> 3 every expert on its chosen tokens -> 4 out[t] = x[t] + sum over the
+    experts e that chose t, in order e = 0..E-1, of p[t,e] * E_e(x_t)
+    (+ the shared experts), the residual carrying a token no expert chose.
+    C defaults to the token-choice capacity ceil(cf * T * k / E) ([P5]), k
+    being the average number of experts per token.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, d = x.shape
+    E = np.asarray(W_g).shape[1]
+    H = logits(x, W_g, b_g, W_noise, eps)
+    if C is None:
+        C = capacity(T, k, E, capacity_factor)
+    ec = expert_choice(H, C)
+    toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    want = set(int(t) for t in toks)
+    contrib = {}
+    for e in range(E):
+        rows = [int(t) for t in ec["sel"][e] if int(t) in want]
+        if not rows:
+            continue
+        y = expert(x[rows], e, act, W1, W3, W2, b1, b2)
+        for i, t in enumerate(rows):
+            contrib[(t, e)] = ec["P"][t, e] * y[i]
+    moe = np.zeros((len(toks), d), dtype=np.float64)
+    for i, t in enumerate(toks):
+        for e in range(E):
+            if ec["chosen"][t, e]:
+                moe[i] += contrib[(int(t), e)]
+    sh = None
+    if shared is not None:
+        sh = shared_experts(x, act, shared["W1s"], shared["W2s"], shared.get("W3s"), shared.get("b1s"),
+                            shared.get("b2s"), tokens=toks)
+        moe = moe + sh
+    return dict(H=H, C=C, tokens=toks, moe=moe, out=x[toks] + moe, shared_out=sh, **ec)
 
 
 def near_ties(H: np.ndarray, k: int, thresh: float = 1e-4) -> dict:

@@ -513,3 +513,89 @@ def test_shared_experts_equal_one_wide_ffn(act):
     a = O.shared_experts(x, act, S["W1s"], S["W2s"], S["W3s"], S["b1s"], S["b2s"])
     b = O.shared_experts(x, act, wide["W1s"], wide["W2s"], wide["W3s"], wide["b1s"], wide["b2s"])
     np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-13)
+
+
+# ---------------------------------------------------------------- expert-choice routing
+
+def _check_top_sets(H, sel):
+    """Definition of an expert's top-C set, checked pair by pair: every chosen
+    token beats every unchosen one (larger score, or equal score and lower index)."""
+    T, E = H.shape
+    for e in range(E):
+        ch = set(int(t) for t in sel[e])
+        assert len(ch) == sel.shape[1] == min(sel.shape[1], T)
+        for t in ch:
+            for u in range(T):
+                if u not in ch:
+                    assert H[t, e] > H[u, e] or (H[t, e] == H[u, e] and t < u), (e, t, u)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_expert_choice_brute_force_with_ties(seed):
+    rng = np.random.default_rng(seed)
+    T, E = 23, 5
+    H = rng.integers(-3, 4, size=(T, E)).astype(np.float64)  # many exact ties
+    for C in [0, 1, 4, 9, 23, 40]:
+        ec = O.expert_choice(H, C)
+        assert ec["sel"].shape == (E, min(C, T))
+        _check_top_sets(H, ec["sel"])
+        assert (np.diff(ec["sel"], axis=1) > 0).all()   # ascending token order
+        np.testing.assert_array_equal(ec["counts"], np.full(E, min(C, T)))  # every expert filled
+        assert ec["dropped"] == int((~ec["chosen"].any(axis=1)).sum())
+
+
+def test_expert_choice_gates_are_router_probabilities():
+    rng = np.random.default_rng(5)
+    H = rng.normal(size=(12, 4))
+    ec = O.expert_choice(H, 5)
+    p = torch.softmax(torch.tensor(H), dim=1).numpy()
+    for e in range(4):
+        for j, t in enumerate(ec["sel"][e]):
+            assert abs(ec["gates"][e, j] - p[t, e]) < 1e-15
+
+
+@pytest.mark.parametrize("act", [O.GELU, O.SWIGLU])
+def test_expert_choice_with_full_capacity_is_dense_softmax_mixture(act):
+    """C >= T: every expert takes every token, so the layer is the dense
+    softmax-weighted mixture sum_e p_e E_e(x) (torch fp64), the same layer
+    as token choice with k = E."""
+    L = _tiny_layer(41, act=act)
+    T, E = L["x"].shape[0], L["W_g"].shape[1]
+    res = O.forward_expert_choice(L["x"], L["W_g"], act, L["W1"], L["W2"], L["W3"], L["b1"], L["b2"],
+                                  b_g=L["b_g"], C=T + 3)
+    x = torch.tensor(L["x"])
+    p = torch.softmax(x @ torch.tensor(L["W_g"]) + torch.tensor(L["b_g"]), dim=1)
+    moe = torch.zeros_like(x)
+    for e in range(E):
+        moe = moe + p[:, e:e + 1] * _torch_ffn(x, act, L["W1"][e], L["W3"][e], L["W2"][e],
+                                               None if L["b1"] is None else L["b1"][e], L["b2"][e])
+    np.testing.assert_allclose(res["moe"], moe.numpy(), rtol=1e-11, atol=1e-12)
+    assert res["dropped"] == 0
+
+
+def test_expert_choice_unchosen_tokens_pass_through_and_multi_expert_tokens_sum():
+    L = _tiny_layer(42, T=30, E=4)
+    res = O.forward_expert_choice(L["x"], L["W_g"], O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"],
+                                  b_g=L["b_g"], C=5)
+    ch = res["chosen"]
+    assert res["dropped"] > 0 and (ch.sum(axis=1) > 1).any()
+    for t in range(30):
+        want = np.zeros(L["x"].shape[1])
+        for e in range(4):
+            if ch[t, e]:
+                want += res["P"][t, e] * O.expert(L["x"][t:t + 1], e, O.GELU, L["W1"], None, L["W2"], L["b1"],
+                                                  L["b2"])[0]
+        np.testing.assert_allclose(res["moe"][t], want, rtol=1e-12, atol=1e-13)
+        if not ch[t].any():
+            np.testing.assert_array_equal(res["out"][t], L["x"][t])
+
+
+def test_expert_choice_capacity_default_and_token_subset():
+    L = _tiny_layer(43, T=40)
+    full = O.forward_expert_choice(L["x"], L["W_g"], O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"],
+                                   b_g=L["b_g"], capacity_factor=1.0, k=2)
+    assert full["C"] == 20  # ceil(1.0 * 40 * 2 / 4)
+    sub = [1, 8, 39]
+    part = O.forward_expert_choice(L["x"], L["W_g"], O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"],
+                                   b_g=L["b_g"], capacity_factor=1.0, k=2, tokens=sub)
+    np.testing.assert_allclose(part["out"], full["out"][sub], rtol=1e-13, atol=1e-14)
