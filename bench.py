@@ -231,7 +231,10 @@ def cpu_oracle_run(w, budget_s: float):
     x, Wg, W1, W2, args = _ORACLE_CACHE[key]
     runs, tokens, t0 = 0, 0, time.perf_counter()
     while True:
-        O.forward(x, Wg, w.k, w.act, W1, W2, **args)
+        if w.routing == "expert":
+            O.forward_expert_choice(x, Wg, w.act, W1, W2, k=w.k, **args)
+        else:
+            O.forward(x, Wg, w.k, w.act, W1, W2, **args)
         runs += 1
         tokens += T_s
         el = time.perf_counter() - t0
@@ -280,6 +283,7 @@ def workload_config(w):
             "act": "swiglu" if w.act == W.ACT_SWIGLU else "gelu", "capacity_factor": w.capacity_factor,
             "noisy_gating": w.noisy, "dtype": w.dtype_name, "seed": w.seed,
             **({"shared_experts": w.n_shared, "d_ff_shared_each": w.F_shared} if w.n_shared else {}),
+            **({"routing": "expert_choice"} if w.routing == "expert" else {}),
             "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
 
 
@@ -310,7 +314,7 @@ def run_ours(a):
     C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
     sw = W.shared_wide(g)
     Fsh = 0 if sw["W1s"] is None else sw["W1s"].shape[0]
-    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act, d_ff_shared=Fsh)
+    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act, d_ff_shared=Fsh, routing=w.routing)
     shared_w = None
     if Fsh:
         b2s = None if sw["b2s_rows"] is None else sw["b2s_rows"].sum(dim=0).contiguous()
@@ -442,7 +446,7 @@ def run_ours(a):
     # ---------------- end to end through the public API with host buffers
     layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
                          b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False,
-                         **(shared_t if Fsh else {}))
+                         routing=w.routing, **(shared_t if Fsh else {}))
     x_host = inp["x"].pin_memory()
     eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
     out_host = torch.empty(w.T, w.d, dtype=w.dtype).pin_memory()
@@ -480,50 +484,53 @@ def run_ours(a):
            "d2h_bytes_per_step": d2h}
 
     # ---------------- routing diagnostics + aux loss of the same batch (moe_routing_stats,
-    # a separate call after the layer): kernel time with L2 flushed before each call
-    logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
-    idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
-    fa = fwd_args()
-    fa[16], fa[23] = P(idx_t), P(logits)
-    _lib.check(lib.moe_forward(*fa), "moe_forward")
-    st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
-    sptr = ctypes.c_void_p(stream.cuda_stream)
-
-    def stats_call():
-        _lib.check(lib.moe_routing_stats(ctypes.byref(shape), P(logits), P(idx_t), P(counts), P(dropped),
-                                         P(st_out[0]), P(st_out[1]), P(st_out[2]), P(ws), ws.numel(), sptr),
-                   "moe_routing_stats")
-
-    for _ in range(3):
-        stats_call()
-    # the call follows the layer, whose router has just written the logits,
-    # so its inputs are L2-resident: time a CUDA graph of n_st back-to-back
-    # calls (no host gaps between launches), after a warm-up replay
+    # a separate call after the layer; token-choice routing only, it needs a top-k table)
+    routing_stats = None
     n_st = 50
-    torch.cuda.synchronize()
-    gst = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gst):
-        sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-        for _ in range(n_st):
-            stats_call()
     sptr = ctypes.c_void_p(stream.cuda_stream)
-    gst.replay()
-    sev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    sev[0].record(stream)
-    gst.replay()
-    sev[1].record(stream)
-    torch.cuda.synchronize()
-    if api.get_device_error(ws) != 0:
-        raise RuntimeError("device-side error in moe_routing_stats")
-    st_ms = sev[0].elapsed_time(sev[1]) / n_st
-    st_bytes = w.T * w.E * 4 + w.T * w.k * 4  # logits + top-k table, read once
-    summ = dict(zip(api.STATS_SUMMARY, st_out[2].tolist()))
-    routing_stats = {"us_per_call": st_ms * 1e3, "timing": f"CUDA graph of {n_st} back-to-back calls, inputs L2-resident",
-                     "algorithmic_bytes": st_bytes,
-                     "achieved_gbs": st_bytes / (st_ms / 1e3) / 1e9,
-                     "frac_hbm": st_bytes / (st_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                     "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
-                     "overflow": summ["overflow"]}
+    if w.routing == "token":
+        logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
+        idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+        fa = fwd_args()
+        fa[16], fa[23] = P(idx_t), P(logits)
+        _lib.check(lib.moe_forward(*fa), "moe_forward")
+        st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
+        sptr = ctypes.c_void_p(stream.cuda_stream)
+
+        def stats_call():
+            _lib.check(lib.moe_routing_stats(ctypes.byref(shape), P(logits), P(idx_t), P(counts), P(dropped),
+                                             P(st_out[0]), P(st_out[1]), P(st_out[2]), P(ws), ws.numel(), sptr),
+                       "moe_routing_stats")
+
+        for _ in range(3):
+            stats_call()
+        # the call follows the layer, whose router has just written the logits,
+        # so its inputs are L2-resident: time a CUDA graph of n_st back-to-back
+        # calls (no host gaps between launches), after a warm-up replay
+        torch.cuda.synchronize()
+        gst = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gst):
+            sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+            for _ in range(n_st):
+                stats_call()
+        sptr = ctypes.c_void_p(stream.cuda_stream)
+        gst.replay()
+        sev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        sev[0].record(stream)
+        gst.replay()
+        sev[1].record(stream)
+        torch.cuda.synchronize()
+        if api.get_device_error(ws) != 0:
+            raise RuntimeError("device-side error in moe_routing_stats")
+        st_ms = sev[0].elapsed_time(sev[1]) / n_st
+        st_bytes = w.T * w.E * 4 + w.T * w.k * 4  # logits + top-k table, read once
+        summ = dict(zip(api.STATS_SUMMARY, st_out[2].tolist()))
+        routing_stats = {"us_per_call": st_ms * 1e3, "timing": f"CUDA graph of {n_st} back-to-back calls, inputs L2-resident",
+                         "algorithmic_bytes": st_bytes,
+                         "achieved_gbs": st_bytes / (st_ms / 1e3) / 1e9,
+                         "frac_hbm": st_bytes / (st_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
+                         "overflow": summ["overflow"]}
 
     # ---------------- the shared experts alone (moe_shared_ffn: two dense GEMMs over
     # every token), kernel time with L2 flushed before each call
@@ -572,10 +579,11 @@ def run_ours(a):
             "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype_name, "data": "synthetic", "config": cfg,
             "stage_ms": {n: statistics.mean(v) for n, v in zip(
-                ["shared_ffn_router_dispatch_gather" if Fsh else "router_dispatch_gather", "expert_gemm1",
+                [("shared_ffn_" if Fsh else "") + ("router_select_gather" if w.routing == "expert"
+                                                     else "router_dispatch_gather"), "expert_gemm1",
                  "expert_gemm2_combine"], stage_ms)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (KERNELS_PER_STEP + (2 if Fsh else 0)) * a.steps,
+            "gpu_launches": (KERNELS_PER_STEP + (2 if Fsh else 0) + (1 if w.routing == "expert" else 0)) * a.steps,
             "clocks": sampler.summary(), "routing_stats": routing_stats}
     if shared_ffn is not None:
         line["shared_ffn"] = shared_ffn

@@ -78,11 +78,18 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
 typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
+/* Token choice: each token takes its top-k experts (steps 2-3 above).
+ * Expert choice: each expert takes its min(C, T) highest-scoring tokens
+ * ("Mixture-of-Experts Sparse Model Scaling", Advanced Theory &
+ * Extensions); see moe_route_expert_choice. */
+typedef enum { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 } moe_routing_t;
 
 /* Shape of one layer call.  T tokens of width d, E experts of hidden width
  * d_ff, top-k routing.  dtype is a moe_dtype_t, act a moe_act_t.
  * d_ff_shared is the hidden width of the shared experts (0 = none; bf16
- * needs a multiple of 64). */
+ * needs a multiple of 64).  routing is a moe_routing_t; with expert choice
+ * k is the average number of experts per token (it sets the capacity) and
+ * T*E < 2^31. */
 typedef struct {
   int64_t T;
   int32_t d;
@@ -92,6 +99,7 @@ typedef struct {
   int32_t dtype;
   int32_t act;
   int32_t d_ff_shared;
+  int32_t routing;
 } moe_shape_t;
 
 /* Shared experts ("Mixture-of-Experts Sparse Model Scaling", Advanced Theory
@@ -122,7 +130,8 @@ typedef struct {
  * not fit in int32. */
 MOE_API int32_t moe_capacity(int64_t T, int32_t k, int32_t E, double capacity_factor);
 
-/* Rows of the expert-grouped buffers for capacity C: min(T*k, E*C). */
+/* Rows of the expert-grouped buffers for capacity C: min(T*k, E*C) with
+ * token choice, E*min(C, T) with expert choice. */
 MOE_API int64_t moe_max_rows(const moe_shape_t* shape, int32_t C);
 
 /* Workspace bytes that moe_forward needs for this shape and capacity (it
@@ -153,6 +162,29 @@ MOE_API moe_status_t moe_route(const moe_shape_t* shape, const void* x, const fl
                        const float* b_g, const float* W_noise, const float* eps,
                        int32_t* idx, float* w, float* logits, int64_t* stats,
                        void* stream);
+
+/* Expert-choice routing (shape->routing == MOE_ROUTE_EXPERT_CHOICE), in
+ * place of steps 2-3: expert e takes the C' = min(C, T) tokens with the
+ * largest router score H[t,e] (ties -> lower token index); the gate of a
+ * chosen (t, e) is the router probability p[t,e] = softmax over all E of
+ * H[t] (not renormalised).  A token may be chosen by no expert (the residual
+ * carries it) or by several ("Mixture-of-Experts Sparse Model Scaling",
+ * Advanced Theory & Extensions).
+ *   C          capacity (moe_capacity with the shape's k, or any C >= 0)
+ *   x, W_g, b_g, W_noise, eps   as in moe_route
+ *   sel      [E,C'] int32 out   chosen tokens of each expert, ascending
+ *   gates    [E,C'] fp32 out    p[t,e] of those pairs
+ *   logits   [T,E] fp32 | NULL  out: the router logits
+ *   dropped  [1] int64 | NULL   out: tokens no expert chose
+ *   ws, ws_bytes  workspace of moe_workspace_size(shape, C)
+ * Selection is exact: the router bounds every fp32 logit's rounding error;
+ * tokens whose order against the C'-th score is not settled by the bounds
+ * are re-scored in fp64, so sel equals the top-C' sets of the exactly
+ * computed scores (up to fp64 rounding). */
+MOE_API moe_status_t moe_route_expert_choice(const moe_shape_t* shape, int32_t C, const void* x,
+                                             const float* W_g, const float* b_g, const float* W_noise,
+                                             const float* eps, int32_t* sel, float* gates, float* logits,
+                                             int64_t* dropped, void* ws, size_t ws_bytes, void* stream);
 
 /* Step 3: capacity-limited dispatch and the gather into expert order.
  *   C         capacity (moe_capacity, or any C >= 0)
@@ -251,6 +283,11 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const floa
  *   shared  moe_shared_t* | NULL: the shared experts' weights, required iff
  *           shape->d_ff_shared > 0; their FFN runs first (on every token)
  *           and its output is added in the combine
+ * With expert-choice routing (shape->routing) the token-choice tables idx,
+ * w, pos must be NULL and stats is untouched; counts (= C' each), offsets
+ * (e*C') and dropped (tokens no expert chose) are written when given, and
+ * out[t] = x[t] + sum over the experts e that chose t, in order e = 0..E-1,
+ * of p[t,e] * E_e(x_t) (+ the shared experts).
  *   out [T,d] dtype out; moe_out [T,d] fp32 | NULL out
  *   idx, w, pos [T,k], counts [E], offsets [E+1], dropped [1], stats [2]:
  *     optional outputs (NULL = keep them in the workspace only; stats as

@@ -16,12 +16,13 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT", 6: "MOE_ERR_BOUNDS"}
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
+MOE_ROUTE_TOKEN_CHOICE, MOE_ROUTE_EXPERT_CHOICE = 0, 1
 
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("d_ff_shared", ctypes.c_int32)]
+                ("d_ff_shared", ctypes.c_int32), ("routing", ctypes.c_int32)]
 
 
 class MoeShared(ctypes.Structure):
@@ -44,6 +45,7 @@ SIGNATURES = {
     "moe_max_rows": (ctypes.c_int64, [_SHAPE, ctypes.c_int32]),
     "moe_workspace_size": (ctypes.c_int, [_SHAPE, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
     "moe_route": (ctypes.c_int, [_SHAPE, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_route_expert_choice": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 10 + [ctypes.c_size_t, _P]),
     "moe_dispatch": (ctypes.c_int, [_SHAPE, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                     ctypes.c_size_t, _P]),
     "moe_dispatch_noalloc": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 10),

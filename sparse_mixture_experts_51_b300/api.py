@@ -13,7 +13,8 @@ from typing import Optional
 import torch
 
 from . import _lib
-from ._lib import MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_BF16, MOE_F32, MoeError, MoeShape, MoeShared
+from ._lib import (MOE_ACT_GELU, MOE_ACT_SWIGLU, MOE_BF16, MOE_F32, MOE_ROUTE_EXPERT_CHOICE, MOE_ROUTE_TOKEN_CHOICE,
+                   MoeError, MoeShape, MoeShared)
 
 ACTS = {"gelu": MOE_ACT_GELU, "swiglu": MOE_ACT_SWIGLU, MOE_ACT_GELU: MOE_ACT_GELU, MOE_ACT_SWIGLU: MOE_ACT_SWIGLU}
 
@@ -41,9 +42,14 @@ def _stream(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def shape_of(T: int, d: int, E: int, k: int, d_ff: int, dtype: torch.dtype, act, d_ff_shared: int = 0) -> MoeShape:
+ROUTINGS = {"token": MOE_ROUTE_TOKEN_CHOICE, "expert": MOE_ROUTE_EXPERT_CHOICE,
+            MOE_ROUTE_TOKEN_CHOICE: MOE_ROUTE_TOKEN_CHOICE, MOE_ROUTE_EXPERT_CHOICE: MOE_ROUTE_EXPERT_CHOICE}
+
+
+def shape_of(T: int, d: int, E: int, k: int, d_ff: int, dtype: torch.dtype, act, d_ff_shared: int = 0,
+             routing="token") -> MoeShape:
     return MoeShape(T=int(T), d=int(d), E=int(E), k=int(k), d_ff=int(d_ff), dtype=_dtype_code(dtype),
-                    act=ACTS[act], d_ff_shared=int(d_ff_shared))
+                    act=ACTS[act], d_ff_shared=int(d_ff_shared), routing=ROUTINGS[routing])
 
 
 def shared_weights(W1s, W2s, W3s=None, b1s=None, b2s=None) -> MoeShared:
@@ -96,6 +102,31 @@ def route(x: torch.Tensor, W_g: torch.Tensor, k: int, b_g=None, W_noise=None, ep
                                _ptr(idx), _ptr(w), _ptr(logits), _ptr(stats), _stream(stream))
     _lib.check(st, "moe_route")
     return idx, w, logits
+
+
+def route_expert_choice(x: torch.Tensor, W_g: torch.Tensor, k: int, C: int, b_g=None, W_noise=None, eps=None,
+                        want_logits: bool = False, ws: Optional[torch.Tensor] = None, stream=None) -> dict:
+    """Expert-choice routing: expert e takes its min(C, T) highest-scoring tokens.
+    Returns sel int32 [E, C'] (ascending token ids), gates fp32 [E, C'],
+    dropped int64 [1] (tokens no expert chose) and logits (or None)."""
+    T, d = x.shape
+    E = W_g.shape[1]
+    shape = shape_of(T, d, E, k, 64, x.dtype, MOE_ACT_GELU, routing="expert")
+    dev = x.device
+    if ws is None:
+        ws = new_workspace(shape, C, dev)
+    Cp = min(int(C), T)
+    out = dict(sel=torch.empty(E, Cp, dtype=torch.int32, device=dev),
+               gates=torch.empty(E, Cp, dtype=torch.float32, device=dev),
+               dropped=torch.empty(1, dtype=torch.int64, device=dev),
+               logits=torch.empty(T, E, dtype=torch.float32, device=dev) if want_logits else None)
+    st = _lib.load().moe_route_expert_choice(ctypes.byref(shape), int(C), _ptr(x), _ptr(W_g), _ptr(b_g),
+                                             _ptr(W_noise), _ptr(eps), _ptr(out["sel"]), _ptr(out["gates"]),
+                                             _ptr(out["logits"]), _ptr(out["dropped"]), _ptr(ws), ws.numel(),
+                                             _stream(stream))
+    _lib.check(st, "moe_route_expert_choice")
+    out["ws"] = ws
+    return out
 
 
 def dispatch(idx: torch.Tensor, x: torch.Tensor, E: int, C: int, d_ff: int = 64, act=MOE_ACT_GELU,
@@ -216,7 +247,7 @@ class MoELayer:
 
     def __init__(self, W_g, W1, W2, k: int, act, W3=None, b_g=None, W_noise=None, b1=None, b2=None,
                  capacity_factor: Optional[float] = None, C: Optional[int] = None, keep_routing: bool = True,
-                 want_moe: bool = False, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None):
+                 want_moe: bool = False, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None, routing="token"):
         if (capacity_factor is None) == (C is None):
             raise ValueError("give exactly one of capacity_factor and C")
         if (W1s is None) != (W2s is None):
@@ -227,6 +258,7 @@ class MoELayer:
         self.E, self.F, self.d = W1.shape
         self.dtype = W1.dtype
         self.Fs = 0 if W1s is None else int(W1s.shape[0])
+        self.routing = ROUTINGS[routing]
         self._shared_t = (W1s, W2s, W3s, b1s, b2s)
         self._shared = shared_weights(W1s, W2s, W3s, b1s, b2s) if W1s is not None else None
         self.capacity_factor, self.C_fixed = capacity_factor, C
@@ -254,7 +286,7 @@ class MoELayer:
         C = self.capacity(T)
         key = (T, C)
         if key not in self._ws:
-            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act, self.Fs)
+            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act, self.Fs, self.routing)
             self._ws[key] = new_workspace(shape, C, self.W1.device)
         return self._ws[key]
 
@@ -262,7 +294,7 @@ class MoELayer:
                  stats: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         T = x.shape[0]
         C = self.capacity(T)
-        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act, self.Fs)
+        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act, self.Fs, self.routing)
         ws = self.workspace(T)
         dev = x.device
         if out is None:
@@ -277,6 +309,9 @@ class MoELayer:
                      offsets=torch.empty(self.E + 1, dtype=torch.int32, device=dev),
                      dropped=torch.empty(1, dtype=torch.int64, device=dev),
                      logits=torch.empty(T, self.E, dtype=torch.float32, device=dev))
+        if r is not None and self.routing == MOE_ROUTE_EXPERT_CHOICE:
+            # the token-choice tables do not exist with expert choice
+            r["idx"] = r["w"] = r["pos"] = None
         g = (lambda n: _ptr(r[n])) if r is not None else (lambda n: None)
         st = _lib.load().moe_forward(
             ctypes.byref(shape), float(self.capacity_factor or 0.0), int(C if self.C_fixed is not None else -1),
@@ -295,10 +330,13 @@ class MoELayer:
         return out
 
     def routing_stats(self, stream=None) -> dict:
-        """Routing diagnostics of the last call (see routing_stats); needs keep_routing."""
+        """Routing diagnostics of the last call (see routing_stats); needs keep_routing
+        and token-choice routing."""
         r = self.last
         if r is None:
             raise RuntimeError("no routing outputs kept: call the layer with keep_routing=True first")
+        if self.routing != MOE_ROUTE_TOKEN_CHOICE:
+            raise ValueError("routing_stats needs a top-k table: token-choice routing only")
         return routing_stats(r["logits"], r["idx"], r["counts"], r["dropped"], ws=r["ws"], stream=stream)
 
 
@@ -331,7 +369,8 @@ def _capture(layer, x, eps, out):
 
 def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=None, b1=None, b2=None,
             capacity_factor: Optional[float] = None, C: Optional[int] = None, want_moe: bool = False,
-            stats: Optional[torch.Tensor] = None, stream=None, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None):
+            stats: Optional[torch.Tensor] = None, stream=None, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None,
+            routing="token"):
     """One-shot whole-layer forward.  Returns (out, routing dict incl. 'moe' when want_moe)."""
     if C is None and capacity_factor is None:
         raise ValueError("give capacity_factor or C")
@@ -339,11 +378,11 @@ def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=No
         capacity_factor = None
     layer = MoELayer(W_g, W1, W2, k, act, W3=W3, b_g=b_g, W_noise=W_noise, b1=b1, b2=b2,
                      capacity_factor=capacity_factor, C=C, keep_routing=True, want_moe=want_moe,
-                     W1s=W1s, W2s=W2s, W3s=W3s, b1s=b1s, b2s=b2s)
+                     W1s=W1s, W2s=W2s, W3s=W3s, b1s=b1s, b2s=b2s, routing=routing)
     out = layer(x, eps=eps, stats=stats, stream=stream)
     return out, layer.last
 
 
 __all__ = ["capacity", "max_rows", "workspace_size", "new_workspace", "get_device_error", "route", "dispatch",
-           "expert_ffn", "shared_ffn", "shared_weights", "combine", "forward", "routing_stats", "stats_summary", "STATS_SUMMARY", "MoELayer",
+           "route_expert_choice", "expert_ffn", "shared_ffn", "shared_weights", "combine", "forward", "routing_stats", "stats_summary", "STATS_SUMMARY", "MoELayer",
            "CapturedForward", "MoeError", "shape_of"]

@@ -54,6 +54,15 @@ struct WsLayout {
   size_t stats_load;    // int32 [kStatsMaxBlocks][E] per-block routed loads
   size_t h_shared;      // [T,d_ff_shared] dtype: hidden activation of the shared experts
   size_t y_shared;      // [T,d] fp32: shared experts' output
+  // expert-choice routing only (zero size otherwise)
+  size_t ec_logits, ec_radius, ec_gate;  // [T,E] fp32
+  size_t ec_lse;                         // [T] fp32
+  size_t ec_row_of;                      // [T,E] int32
+  size_t ec_flag;                        // [E,T] uint8
+  size_t ec_band;                        // [E,T] int32
+  size_t ec_h64;                         // [E,T] fp64
+  size_t ec_sel;                         // [E*Cp] int32
+  int32_t ec_cp;                         // min(C, T)
   size_t idx, w, pos;        // [T,k] int32 / fp32 / int32
   size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
   size_t counts, offsets;    // [E], [E+1] int32
@@ -89,9 +98,11 @@ struct RouterParams {
   const float* W_n;
   const float* eps;
   int T, d, E, k;
-  int32_t* idx;
+  int32_t* idx;     // [T,k] out; null: no top-k (expert-choice routing: logits, radius and lse only)
   float* w;
   float* logits;
+  float* radius;    // [T,E] out or null: a rigorous bound on |logit - exact logit|
+  float* lse;       // [T] out or null: log-sum-exp of the token's fp32 logits
   long long* stats;
   int* err;
 };
@@ -166,6 +177,32 @@ struct CombineParams {
   int* err;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st);
+
+// Expert-choice routing (expert_choice.cu): each expert takes its Cp = min(C, T)
+// highest-scoring tokens; rows e*Cp .. e*Cp+Cp-1 of the grouped buffers are
+// expert e's tokens in token order.
+struct EcParams {
+  const float* logits;  // [T,E] fp32 router logits
+  const float* radius;  // [T,E] their error radii
+  const float* lse;     // [T]
+  const void* x;        // [T,d] tokens (fp64 re-evaluation of the band)
+  const float* W_g;
+  const float* b_g;
+  const float* W_n;
+  const float* eps;
+  int T, d, E, Cp;
+  int32_t* sel;      // [E*Cp] out: token of each grouped row
+  int32_t* row_of;   // [T,E] out: grouped row of (t, e), -1 if e did not choose t
+  float* gate_te;    // [T,E] out: p[t,e] where chosen
+  uint8_t* flag;     // [E][T] scratch
+  int32_t* band;     // [E][T] scratch
+  double* h64;       // [E][T] scratch
+  int* err;
+};
+cudaError_t launch_ec_select(const EcParams& p, int dtype, cudaStream_t st);
+cudaError_t launch_ec_finalize(const EcParams& p, int32_t* counts, int32_t* offsets, long long* dropped,
+                               cudaStream_t st);
+cudaError_t launch_ec_gather(const EcParams& p, const void* x, void* x_perm, int elem_bytes, cudaStream_t st);
 
 struct StatsParams {
   const float* logits;     // [T,E]

@@ -23,7 +23,9 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   WsLayout L{};
   const long long Tk = s.T * s.k;
   const long long EC = static_cast<long long>(s.E) * C;
-  L.rows = Tk < EC ? Tk : EC;
+  const bool ec = s.routing == MOE_ROUTE_EXPERT_CHOICE;
+  L.ec_cp = static_cast<int32_t>(C < s.T ? C : s.T);
+  L.rows = ec ? static_cast<long long>(s.E) * L.ec_cp : (Tk < EC ? Tk : EC);
   L.nblk_dispatch = dispatch_nblk(Tk);
   const size_t b = dtype_bytes(s.dtype);
   size_t o = 0;
@@ -42,6 +44,16 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   // (the regions up to here do not depend on C: any C's workspace holds them)
   L.h_shared = take(b * static_cast<size_t>(s.T) * s.d_ff_shared);
   L.y_shared = take(s.d_ff_shared > 0 ? sizeof(float) * static_cast<size_t>(s.T) * s.d : 0);
+  const size_t TE = ec ? static_cast<size_t>(s.T) * s.E : 0;
+  L.ec_logits = take(sizeof(float) * TE);
+  L.ec_radius = take(sizeof(float) * TE);
+  L.ec_gate = take(sizeof(float) * TE);
+  L.ec_lse = take(ec ? sizeof(float) * static_cast<size_t>(s.T) : 0);
+  L.ec_row_of = take(sizeof(int32_t) * TE);
+  L.ec_flag = take(TE);
+  L.ec_band = take(sizeof(int32_t) * TE);
+  L.ec_h64 = take(sizeof(double) * TE);
+  L.ec_sel = take(ec ? sizeof(int32_t) * static_cast<size_t>(L.rows) : 0);
   L.idx = take(sizeof(int32_t) * Tk);
   L.w = take(sizeof(float) * Tk);
   L.pos = take(sizeof(int32_t) * Tk);
@@ -70,6 +82,9 @@ moe_status_t check_shape(const moe_shape_t* s) {
   if (s->dtype == MOE_F32 && s->d % 4 != 0) return MOE_ERR_UNSUPPORTED;
   if (s->d_ff_shared < 0) return MOE_ERR_INVALID_ARG;
   if (s->dtype == MOE_BF16 && s->d_ff_shared % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  if (s->routing != MOE_ROUTE_TOKEN_CHOICE && s->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (s->routing == MOE_ROUTE_EXPERT_CHOICE && s->T * static_cast<long long>(s->E) >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -102,9 +117,7 @@ int32_t moe_capacity(int64_t T, int32_t k, int32_t E, double capacity_factor) {
 
 int64_t moe_max_rows(const moe_shape_t* shape, int32_t C) {
   if (check_shape(shape) == MOE_ERR_INVALID_ARG || C < 0) return -1;
-  const long long Tk = shape->T * shape->k;
-  const long long EC = static_cast<long long>(shape->E) * C;
-  return Tk < EC ? Tk : EC;
+  return ws_layout(*shape, C).rows;
 }
 
 moe_status_t moe_workspace_size(const moe_shape_t* shape, int32_t C, size_t* bytes) {
@@ -140,6 +153,64 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g
   p.stats = reinterpret_cast<long long*>(stats);
   p.err = nullptr;
   return cuda_status(launch_router(p, shape->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+// Expert-choice routing: the router in its no-top-k mode (logits, radii,
+// log-sum-exp), then every expert's exact top-C' selection.
+static moe_status_t ec_route_impl(const moe_shape_t* shape, const void* x, const float* W_g, const float* b_g,
+                                  const float* W_noise, const float* eps, float* logits, void* ws, const WsLayout& L,
+                                  cudaStream_t st, EcParams& ep) {
+  if (logits == nullptr) logits = at<float>(ws, L.ec_logits);
+  RouterParams p{};
+  p.x = x;
+  p.W_g = W_g;
+  p.b_g = b_g;
+  p.W_n = W_noise;
+  p.eps = eps;
+  p.T = static_cast<int>(shape->T);
+  p.d = shape->d;
+  p.E = shape->E;
+  p.k = shape->k;
+  p.idx = nullptr;
+  p.w = nullptr;
+  p.logits = logits;
+  p.radius = at<float>(ws, L.ec_radius);
+  p.lse = at<float>(ws, L.ec_lse);
+  p.stats = nullptr;
+  p.err = at<int>(ws, L.err);
+  if (shape->T > 0) {
+    cudaError_t e = launch_router(p, shape->dtype, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  ep = EcParams{};
+  ep.logits = logits;
+  ep.radius = p.radius;
+  ep.lse = p.lse;
+  ep.x = x;
+  ep.W_g = W_g;
+  ep.b_g = b_g;
+  ep.W_n = W_noise;
+  ep.eps = eps;
+  ep.T = static_cast<int>(shape->T);
+  ep.d = shape->d;
+  ep.E = shape->E;
+  ep.Cp = L.ec_cp;
+  ep.sel = at<int32_t>(ws, L.ec_sel);
+  ep.row_of = at<int32_t>(ws, L.ec_row_of);
+  ep.gate_te = at<float>(ws, L.ec_gate);
+  ep.flag = at<uint8_t>(ws, L.ec_flag);
+  ep.band = at<int32_t>(ws, L.ec_band);
+  ep.h64 = at<double>(ws, L.ec_h64);
+  ep.err = at<int>(ws, L.err);
+  return cuda_status(launch_ec_select(ep, shape->dtype, st));
+}
+
+// gates of the chosen pairs in [E, C'] order: gates[row] = gate_te[sel[row], e]
+__global__ void ec_gates_kernel(const int32_t* sel, const float* gate_te, int E, int Cp, float* gates) {
+  const long long row = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (row >= static_cast<long long>(E) * Cp) return;
+  const int e = static_cast<int>(row / Cp);
+  gates[row] = gate_te[static_cast<long long>(sel[row]) * E + e];
 }
 
 static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x,
@@ -183,11 +254,46 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int
   return cuda_status(launch_gather(gp, st));
 }
 
+moe_status_t moe_route_expert_choice(const moe_shape_t* shape, int32_t C, const void* x, const float* W_g,
+                                     const float* b_g, const float* W_noise, const float* eps, int32_t* sel,
+                                     float* gates, float* logits, int64_t* dropped, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->routing != MOE_ROUTE_EXPERT_CHOICE || C < 0) return MOE_ERR_INVALID_ARG;
+  if (W_g == nullptr) return MOE_ERR_INVALID_ARG;
+  if ((W_noise == nullptr) != (eps == nullptr)) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*shape, C);
+  if (shape->T > 0 && x == nullptr) return MOE_ERR_INVALID_ARG;
+  if (L.rows > 0 && (sel == nullptr || gates == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (shape->T > 0 && !aligned16(x)) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EcParams ep{};
+  if ((st = ec_route_impl(shape, x, W_g, b_g, W_noise, eps, logits, ws, L, s, ep)) != MOE_OK) return st;
+  if (L.rows > 0) {
+    if (cudaMemcpyAsync(sel, ep.sel, sizeof(int32_t) * static_cast<size_t>(L.rows), cudaMemcpyDeviceToDevice, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    ec_gates_kernel<<<static_cast<unsigned>((L.rows + 255) / 256), 256, 0, s>>>(ep.sel, ep.gate_te, shape->E,
+                                                                                 L.ec_cp, gates);
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (dropped != nullptr) {
+    // counts / offsets are implied (C' each): the workspace copies take them
+    if (shape->T == 0) return cuda_status(cudaMemsetAsync(dropped, 0, sizeof(int64_t), s));
+    return cuda_status(launch_ec_finalize(ep, at<int32_t>(ws, L.counts), at<int32_t>(ws, L.offsets),
+                                          reinterpret_cast<long long*>(dropped), s));
+  }
+  return MOE_OK;
+}
+
 moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x, int32_t* pos,
                           int32_t* counts, int32_t* offsets, int64_t* dropped, void* x_perm, int32_t* row_token,
                           void* ws, size_t ws_bytes, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
+  if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;  // token-choice tables
   if (C < 0) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
@@ -204,6 +310,7 @@ moe_status_t moe_testing_dispatch_stalled(const moe_shape_t* shape, int32_t C, c
                                           size_t ws_bytes, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
+  if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;  // token-choice tables
   if (C < 0 || counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*shape, C);
@@ -333,6 +440,7 @@ moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const float* y_per
                          const float* y_shared, void* out, float* moe_out, void* stream) {
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
+  if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;  // token-choice tables
   if (C < 0) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (idx == nullptr || w == nullptr || pos == nullptr || offsets == nullptr || out == nullptr))
     return MOE_ERR_INVALID_ARG;
@@ -383,6 +491,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     if (stage_events == nullptr || stage_events[i] == nullptr) return MOE_OK;
     return cuda_status(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(stage_events[i]), s, rec_flags));
   };
+  const bool ec = shape->routing == MOE_ROUTE_EXPERT_CHOICE;
+  if (ec && (idx != nullptr || w != nullptr || pos != nullptr)) return MOE_ERR_INVALID_ARG;
   if (idx == nullptr) idx = at<int32_t>(ws, L.idx);
   if (w == nullptr) w = at<float>(ws, L.w);
   if (pos == nullptr) pos = at<int32_t>(ws, L.pos);
@@ -397,12 +507,37 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     y_sh = at<float>(ws, L.y_shared);
     if ((st = shared_impl(shape, x, shared, y_sh, ws, L, s)) != MOE_OK) return st;
   }
-  if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, stream)) != MOE_OK) return st;
-  if ((st = mark(1)) != MOE_OK) return st;
   int32_t* row_of = at<int32_t>(ws, L.row_of);
-  if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
-                          s, -1, row_of)) != MOE_OK)
-    return st;
+  const float* gate = w;
+  moe_shape_t cshape = *shape;  // the combine's view: k ranks per token
+  if (ec) {
+    EcParams ep{};
+    if ((st = ec_route_impl(shape, x, W_g, b_g, W_noise, eps, logits, ws, L, s, ep)) != MOE_OK) return st;
+    if ((st = mark(1)) != MOE_OK) return st;
+    if (shape->T == 0) {
+      if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * shape->E, s) != cudaSuccess ||
+          cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (shape->E + 1), s) != cudaSuccess ||
+          cudaMemsetAsync(dropped, 0, sizeof(int64_t), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else {
+      if ((st = cuda_status(launch_ec_finalize(ep, counts, offsets, reinterpret_cast<long long*>(dropped), s))) !=
+          MOE_OK)
+        return st;
+      if ((st = cuda_status(launch_ec_gather(ep, x, at<void>(ws, L.x_perm),
+                                             static_cast<int>(dtype_bytes(shape->dtype)), s))) != MOE_OK)
+        return st;
+    }
+    // the combine sees every expert as a "rank" of each token: row_of [T,E], gates [T,E]
+    row_of = ep.row_of;
+    gate = ep.gate_te;
+    cshape.k = shape->E;
+  } else {
+    if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, stream)) != MOE_OK) return st;
+    if ((st = mark(1)) != MOE_OK) return st;
+    if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
+                            s, -1, row_of)) != MOE_OK)
+      return st;
+  }
   if ((st = mark(2)) != MOE_OK) return st;
   float* y_perm = at<float>(ws, L.y_perm);
   FfnParams fp{};
@@ -429,7 +564,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     if ((st = mark(3)) != MOE_OK) return st;
   }
   if ((st = mark(4)) != MOE_OK) return st;
-  if ((st = combine_impl(shape, L.rows, y_perm, idx, w, pos, offsets, x, y_sh, out, moe_out, at<int>(ws, L.err), s,
+  if ((st = combine_impl(&cshape, L.rows, y_perm, idx, gate, pos, offsets, x, y_sh, out, moe_out, at<int>(ws, L.err), s,
                         row_of)) != MOE_OK)
     return st;
   return mark(5);

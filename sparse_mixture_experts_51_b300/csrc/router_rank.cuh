@@ -166,7 +166,23 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
       if (h != h) h = -INFINITY;  // NaN ranks last
       H[s] = h;
       B[s] = bound * 1.25f + 1e-30f;
+      if (p.radius) p.radius[t * E + e] = B[s];
     }
+  }
+  if (p.idx == nullptr) {
+    // expert-choice routing: no per-token top-k; the log-sum-exp of the
+    // token's logits gives the router probabilities exp(h - lse)
+    float m = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) m = fmaxf(m, H[s]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float sum = 0.f;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) sum += (lane + 32 * s < E && m > -INFINITY) ? expf(H[s] - m) : 0.f;
+    sum = warp_sum(sum);
+    if (lane == 0 && p.lse) p.lse[t] = m > -INFINITY ? m + logf(sum) : -INFINITY;
+    return;
   }
 
   // top-k by fp32 value (ties -> lower index), carrying the bounds; lane r < k

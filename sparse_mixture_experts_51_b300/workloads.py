@@ -13,9 +13,10 @@ Shapes follow the five layer configurations this library is measured on:
   switch_top1     T=32768 d=768  E=64 k=1 GELU   F=3072  cf=1.0   bf16,
                   Zipf router bias and noisy gating
   decode_t128     T=128   d=2048 E=64 k=6 SwiGLU F=1408  cf=2.0   bf16
-and one layer with shared experts (the next-step extension):
+and two layers for the next-step extensions:
   shared_t4096    T=4096  d=2048 E=64 k=6 SwiGLU F=1408  cf=1.25  bf16,
                   plus 2 shared experts of width 1408
+  ec_t4096        bf16_t4096's layer and tokens with expert-choice routing
 
 Value recipe (all draws fp32 standard normal from one CPU torch.Generator
 seeded per workload, scaled, then cast to the storage dtype):
@@ -60,6 +61,7 @@ class Workload:
     weight_std_literal_d: bool = False  # every weight ~N(0,1/d)
     n_shared: int = 0        # shared experts (every token, weight 1)
     F_shared: int = 0        # hidden width of each shared expert
+    routing: str = "token"   # "token" (top-k per token) or "expert" (top-C tokens per expert)
 
     @property
     def dtype_name(self) -> str:
@@ -93,6 +95,9 @@ WORKLOADS = {
     # same width (the DeepSeek-MoE layout, at a prefill-sized batch)
     "shared_t4096": Workload("shared_t4096", T=4096, d=2048, E=64, k=6, F=1408, act=ACT_SWIGLU,
                              capacity_factor=1.25, dtype=torch.bfloat16, seed=6, n_shared=2, F_shared=1408),
+    # the bench layer and tokens with expert-choice routing at the same capacity (1280 tokens per expert)
+    "ec_t4096": Workload("ec_t4096", T=4096, d=1024, E=8, k=2, F=4096, act=ACT_SWIGLU,
+                         capacity_factor=1.25, dtype=torch.bfloat16, seed=1, routing="expert"),
 }
 ORDER = ["tiny_fp32", "bf16_t4096", "mixtral_t16384", "switch_top1", "decode_t128"]
 

@@ -205,3 +205,32 @@ def test_shared_expert_argument_errors(lib):
     bad = list(args)
     bad[10] = addr(gelu_w)
     assert lib.moe_forward(ctypes.byref(s0), 1.25, -1, *bad, f, nf, None) == INVALID
+
+
+@no_gpu
+def test_expert_choice_argument_errors(lib):
+    f = P(FAKE)
+    tc = _shape()                      # token choice, T=64, E=4, k=2
+    ec = _shape(routing=1)
+    assert lib.moe_max_rows(ctypes.byref(ec), 40) == 4 * 40
+    assert lib.moe_max_rows(ctypes.byref(ec), 100) == 4 * 64   # C' = min(C, T)
+    assert _ws(lib, _shape(routing=7), 40)[0] == INVALID
+    assert _ws(lib, _shape(routing=1, T=1 << 27, E=32, k=1), 40)[0] == UNSUPPORTED  # T*E >= 2^31
+    st, n = _ws(lib, ec, 40)
+    assert st == OK and n > _ws(lib, tc, 40)[1]
+    # the expert-choice route needs an expert-choice shape, its outputs and a workspace
+    assert lib.moe_route_expert_choice(ctypes.byref(tc), 40, f, f, None, None, None, f, f, None, None, f, n,
+                                       None) == INVALID
+    assert lib.moe_route_expert_choice(ctypes.byref(ec), 40, f, f, None, None, None, None, f, None, None, f, n,
+                                       None) == INVALID
+    assert lib.moe_route_expert_choice(ctypes.byref(ec), 40, f, f, None, f, None, f, f, None, None, f, n,
+                                       None) == INVALID  # W_noise without eps
+    assert lib.moe_route_expert_choice(ctypes.byref(ec), 40, f, f, None, None, None, f, f, None, None, f,
+                                       _ws(lib, tc, 40)[1], None) == WORKSPACE
+    # token-choice steps refuse an expert-choice shape
+    assert lib.moe_dispatch(ctypes.byref(ec), 40, f, f, f, f, f, f, f, None, f, n, None) == INVALID
+    assert lib.moe_combine(ctypes.byref(ec), 40, f, f, f, f, f, None, None, f, None, None) == INVALID
+    # the forward takes no token-choice tables with expert choice
+    args = [f, f, None, None, None, f, None, f, None, None, None, f, None, f, None, None, None, None, None, None,
+            None]
+    assert lib.moe_forward(ctypes.byref(ec), 1.25, -1, *args, f, n, None) == INVALID
