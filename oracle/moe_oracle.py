@@ -109,6 +109,14 @@ def gates(H: np.ndarray, idx: np.ndarray) -> np.ndarray:
     return z / z.sum(axis=1, keepdims=True)
 
 
+def gates_raw(H: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """Un-renormalised gates: w[t,r] = p_i(x) for i = idx[t,r], the full
+    softmax over all experts ([P1] "Mathematical Formulation": the layer
+    output weights each selected expert by its routing probability)."""
+    P = softmax_rows(H)
+    return np.take_along_axis(P, np.asarray(idx, dtype=np.int64), axis=1)
+
+
 def capacity(T: int, k: int, E: int, capacity_factor: float) -> int:
     """Expert capacity C = ceil(factor * tokens * k / experts) ([P5] Capacity
     card; [P4] s3 gives the k=1 form)."""
@@ -189,6 +197,51 @@ def expert_choice(H: np.ndarray, C: int) -> dict:
     counts = np.full(E, Cp, dtype=np.int64)
     dropped = int(T - np.count_nonzero(chosen.any(axis=1)))
     return dict(sel=sel, gates=gates, chosen=chosen, counts=counts, dropped=dropped, P=P)
+
+
+def reroute(idx: np.ndarray, disp: dict, backup: np.ndarray, C: int) -> dict:
+    """Overflow re-routing to a backup expert ([P2] "Capacity limits make
+    dispatch observable" and "Overflow handling defines an output contract":
+    a full expert's assignment may be sent to a backup, lower-ranked expert;
+    [P3]: routed to a secondary expert).
+
+    Readings: a token's backup is its (k+1)-th ranked expert (``backup[t]``,
+    -1 when k = E); only the token's first dropped assignment (lowest rank)
+    asks for it, since an expert takes a token once; the requests are served
+    after the capacity dispatch, first-come in the same priority order (rank
+    r, then token t), while the backup has fewer than C assignments; a
+    rerouted assignment keeps its gate; the rest stay dropped.
+
+    Returns idx (the expert each assignment is finally sent to), pos, counts,
+    offsets, dropped (after re-routing) and rerouted (how many were moved).
+    """
+    idx = np.array(idx, dtype=np.int64, copy=True)
+    pos = np.array(disp["pos"], dtype=np.int64, copy=True)
+    T, k = idx.shape
+    E = len(disp["counts"])
+    load = np.array(disp["counts"], dtype=np.int64, copy=True)
+    first = {}
+    for t in range(T):
+        for r in range(k):
+            if pos[t, r] < 0:
+                first[t] = r
+                break
+    rerouted = 0
+    for r in range(k):          # priority order: rank, then token
+        for t in range(T):
+            if first.get(t) != r:
+                continue
+            e = int(backup[t])
+            if e >= 0 and load[e] < C:
+                idx[t, r] = e
+                pos[t, r] = load[e]
+                load[e] += 1
+                rerouted += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + load[e]
+    dropped = int(np.count_nonzero(pos < 0))
+    return dict(idx=idx, pos=pos, counts=load, offsets=offsets, dropped=dropped, rerouted=rerouted)
 
 
 # --------------------------------------------------------------------------
@@ -288,7 +341,8 @@ def combine(x, idx, w, pos, expert_out, residual=True, tokens=None, shared_out=N
 
 def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
             b_g=None, W_noise=None, eps=None, capacity_factor: Optional[float] = None,
-            C: Optional[int] = None, tokens=None, idx_override=None, shared: Optional[dict] = None) -> dict:
+            C: Optional[int] = None, tokens=None, idx_override=None, shared: Optional[dict] = None,
+            gate_mode: str = "renorm", overflow: str = "drop") -> dict:
     """Forward pass of one sparse MoE layer, step by step.
 
     1 logits ([P4] s2) -> 2 top-k ([P4] s2) -> 3 gates ([P4] s2) ->
@@ -296,7 +350,9 @@ def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
     assignments -> 7 combine + residual ([P4] s1, s3).
     ``shared``: optional shared experts (keys W1s, W2s and optionally W3s,
     b1s, b2s, as in ``shared_experts``), applied to every token and added in
-    the combine.
+    the combine.  ``gate_mode``: "renorm" (softmax over the k selected
+    logits) or "raw" (``gates_raw``).  ``overflow``: "drop" or "reroute"
+    (``reroute``, after the dispatch).
 
     ``tokens``: evaluate experts and combine only for these token ids
     (routing and dispatch always cover the whole batch, since capacity
@@ -309,10 +365,16 @@ def forward(x, W_g, k: int, act: int, W1, W2, W3=None, b1=None, b2=None,
     E = np.asarray(W_g).shape[1]
     H = logits(x, W_g, b_g, W_noise, eps)
     idx = topk(H, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
-    w = gates(H, idx)
+    w = gates(H, idx) if gate_mode == "renorm" else gates_raw(H, idx)
     if C is None:
         C = capacity(T, k, E, capacity_factor)
     disp = dispatch(idx, E, C)
+    if overflow == "reroute":
+        backup = topk(H, k + 1)[:, k] if k < E else np.full(T, -1, dtype=np.int64)
+        rr = reroute(idx, disp, backup, C)
+        idx = rr["idx"]
+        disp = dict(disp, pos=rr["pos"], counts=rr["counts"], offsets=rr["offsets"], dropped=rr["dropped"],
+                    rerouted=rr["rerouted"], backup=backup)
     pos = disp["pos"]
     toks = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     per_expert = [[] for _ in range(E)]

@@ -599,3 +599,86 @@ def test_expert_choice_capacity_default_and_token_subset():
     part = O.forward_expert_choice(L["x"], L["W_g"], O.GELU, L["W1"], L["W2"], None, L["b1"], L["b2"],
                                    b_g=L["b_g"], capacity_factor=1.0, k=2, tokens=sub)
     np.testing.assert_allclose(part["out"], full["out"][sub], rtol=1e-13, atol=1e-14)
+
+
+# ---------------------------------------------------------------- overflow variants
+
+def test_reroute_worked_example():
+    """The worked capacity example of "Mixture-of-experts Models" (top-1
+    assignments [0,0,0,1,1,2,3,3], capacity 2: the third token overflows
+    expert 0), with per-token backups: the overflow goes to its backup when
+    that expert has room, and stays dropped when it is full.  Values worked
+    by hand."""
+    idx = np.array([[0], [0], [0], [1], [1], [2], [3], [3]])
+    disp = O.dispatch(idx, 4, 2)
+    assert disp["dropped"] == 1 and list(disp["counts"]) == [2, 2, 1, 2]
+    rr = O.reroute(idx, disp, np.array([1, 2, 2, 0, 3, 3, 2, 0]), 2)
+    assert rr["idx"][:, 0].tolist() == [0, 0, 2, 1, 1, 2, 3, 3]
+    assert rr["pos"][:, 0].tolist() == [0, 1, 1, 0, 1, 0, 0, 1]
+    assert rr["counts"].tolist() == [2, 2, 2, 2] and rr["offsets"].tolist() == [0, 2, 4, 6, 8]
+    assert rr["dropped"] == 0 and rr["rerouted"] == 1
+    full = O.reroute(idx, disp, np.array([1, 2, 1, 0, 3, 3, 2, 0]), 2)  # token 2's backup (1) is full
+    assert full["idx"][2, 0] == 0 and full["pos"][2, 0] == -1 and full["dropped"] == 1 and full["rerouted"] == 0
+
+
+def test_reroute_through_the_layer_uses_the_next_ranked_expert():
+    """Logits built so every token's ranking is known: the backup is the
+    (k+1)-th expert of the token's own ranking."""
+    T, E = 8, 4
+    top = [0, 0, 0, 1, 1, 2, 3, 3]
+    nxt = [1, 2, 2, 0, 3, 3, 2, 0]
+    H = np.zeros((T, E))
+    for t in range(T):
+        H[t, top[t]] = 10.0
+        H[t, nxt[t]] = 5.0
+    # identity-like x and W_g so that logits == H exactly
+    x = np.eye(T)
+    res = O.forward(x, H, 1, O.GELU, np.zeros((E, 2, T)), np.zeros((E, T, 2)), C=2, overflow="reroute")
+    assert res["idx"][:, 0].tolist() == [0, 0, 2, 1, 1, 2, 3, 3]
+    assert res["dropped"] == 0 and res["rerouted"] == 1
+    np.testing.assert_array_equal(res["backup"], nxt)
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_reroute_invariants(seed):
+    rng = np.random.default_rng(seed)
+    T, E, k, C = 40, 6, 2, 9
+    H = rng.normal(size=(T, E)) + np.linspace(2, 0, E)  # skewed: drops happen
+    idx0 = O.topk(H, k)
+    disp = O.dispatch(idx0, E, C)
+    backup = O.topk(H, k + 1)[:, k]
+    rr = O.reroute(idx0, disp, backup, C)
+    assert disp["dropped"] > 0
+    assert (rr["counts"] <= C).all() and rr["counts"].sum() + rr["dropped"] == T * k
+    assert rr["dropped"] == disp["dropped"] - rr["rerouted"]
+    for t in range(T):
+        assert len(set(rr["idx"][t][rr["pos"][t] >= 0])) == int((rr["pos"][t] >= 0).sum())  # no expert twice
+        for r in range(k):
+            if rr["idx"][t, r] != idx0[t, r]:           # moved: only the first dropped rank, to the backup
+                assert rr["idx"][t, r] == backup[t] and disp["pos"][t, r] < 0
+                assert all(disp["pos"][t, q] >= 0 for q in range(r))
+            elif rr["pos"][t, r] < 0 and all(disp["pos"][t, q] >= 0 for q in range(r)):
+                assert rr["counts"][backup[t]] == C   # a refused request found its backup full
+    # the rows of each expert are numbered 0..counts-1 without gaps
+    for e in range(E):
+        slots = sorted(rr["pos"][(rr["idx"] == e) & (rr["pos"] >= 0)].tolist())
+        assert slots == list(range(rr["counts"][e]))
+    # with room for everything, re-routing changes nothing
+    big = O.dispatch(idx0, E, T * k)
+    same = O.reroute(idx0, big, backup, T * k)
+    np.testing.assert_array_equal(same["idx"], idx0)
+    assert same["rerouted"] == 0
+
+
+def test_raw_gates_are_routing_probabilities():
+    rng = np.random.default_rng(7)
+    H = rng.normal(size=(10, 5))
+    idx = O.topk(H, 2)
+    p = torch.softmax(torch.tensor(H), dim=1).numpy()
+    w = O.gates_raw(H, idx)
+    np.testing.assert_allclose(w, np.take_along_axis(p, idx, axis=1), rtol=1e-15, atol=0)
+    assert (w.sum(axis=1) < 1).all()
+    # renormalising the raw gates gives the default gates
+    np.testing.assert_allclose(w / w.sum(axis=1, keepdims=True), O.gates(H, idx), rtol=1e-13, atol=1e-15)
+    # k = E: the raw gates are the whole distribution
+    np.testing.assert_allclose(O.gates_raw(H, O.topk(H, 5)).sum(axis=1), 1.0, rtol=1e-14)
