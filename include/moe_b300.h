@@ -83,13 +83,29 @@ typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
  * ("Mixture-of-Experts Sparse Model Scaling", Advanced Theory &
  * Extensions); see moe_route_expert_choice. */
 typedef enum { MOE_ROUTE_TOKEN_CHOICE = 0, MOE_ROUTE_EXPERT_CHOICE = 1 } moe_routing_t;
+/* Gates of the selected experts (token choice): renormalised over the k
+ * selected (the default), or the raw routing probabilities p_i, the full
+ * softmax over all E ("Mixture-of-Experts Sparse Model Scaling",
+ * Mathematical Formulation, the displayed top-k output). */
+typedef enum { MOE_GATES_RENORM = 0, MOE_GATES_RAW = 1 } moe_gates_t;
+/* An assignment over capacity (token choice): dropped (the default), or
+ * re-routed to the token's backup expert, its (k+1)-th ranked one, when that
+ * expert has room ("Mixture-of-experts Models", Level 2, "Capacity limits
+ * make dispatch observable" and "Overflow handling defines an output
+ * contract").  Only the token's first dropped assignment asks for the
+ * backup; requests are served after the capacity dispatch, first-come in the
+ * same priority order (rank, then token); a re-routed assignment keeps its
+ * gate.  Available through moe_forward. */
+typedef enum { MOE_OVERFLOW_DROP = 0, MOE_OVERFLOW_REROUTE = 1 } moe_overflow_t;
 
 /* Shape of one layer call.  T tokens of width d, E experts of hidden width
  * d_ff, top-k routing.  dtype is a moe_dtype_t, act a moe_act_t.
  * d_ff_shared is the hidden width of the shared experts (0 = none; bf16
  * needs a multiple of 64).  routing is a moe_routing_t; with expert choice
  * k is the average number of experts per token (it sets the capacity) and
- * T*E < 2^31. */
+ * T*E < 2^31.  gates (moe_gates_t) and overflow (moe_overflow_t) apply to
+ * token choice; with expert choice both must be 0 (its gates are the
+ * routing probabilities by definition and nothing overflows). */
 typedef struct {
   int64_t T;
   int32_t d;
@@ -100,6 +116,8 @@ typedef struct {
   int32_t act;
   int32_t d_ff_shared;
   int32_t routing;
+  int32_t gates;
+  int32_t overflow;
 } moe_shape_t;
 
 /* Shared experts ("Mixture-of-Experts Sparse Model Scaling", Advanced Theory
@@ -148,7 +166,9 @@ MOE_API moe_status_t moe_workspace_size(const moe_shape_t* shape, int32_t C, siz
  *   W_noise  [d,E]  fp32 | NULL  noise projection; with eps, adds
  *   eps      [T,E]  fp32 | NULL  eps * softplus(x W_noise) to the logits
  *   idx      [T,k]  int32 out    selected experts, largest logit first
- *   w        [T,k]  fp32  out    gates (softmax over the selected logits)
+ *   w        [T,k]  fp32  out    gates (softmax over the selected logits;
+ *                                 with shape->gates = MOE_GATES_RAW the
+ *                                 full-softmax probabilities p_i)
  *   logits   [T,E]  fp32 | NULL  out: the (noisy) logits, computed in fp32
  *   stats    [2]    int64 | NULL out, ADDED to: [0] tokens whose selection
  *                   was settled by the fp64 re-evaluation, [1] tokens whose
@@ -283,6 +303,9 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const floa
  *   shared  moe_shared_t* | NULL: the shared experts' weights, required iff
  *           shape->d_ff_shared > 0; their FFN runs first (on every token)
  *           and its output is added in the combine
+ * With overflow re-routing (shape->overflow) idx holds, for each
+ * assignment, the expert it was finally sent to (the backup for a re-routed
+ * one), pos its slot there, dropped the assignments left without an expert.
  * With expert-choice routing (shape->routing) the token-choice tables idx,
  * w, pos must be NULL and stats is untouched; counts (= C' each), offsets
  * (e*C') and dropped (tokens no expert chose) are written when given, and

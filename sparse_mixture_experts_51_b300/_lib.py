@@ -17,12 +17,15 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 MOE_F32, MOE_BF16 = 0, 1
 MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_ROUTE_TOKEN_CHOICE, MOE_ROUTE_EXPERT_CHOICE = 0, 1
+MOE_GATES_RENORM, MOE_GATES_RAW = 0, 1
+MOE_OVERFLOW_DROP, MOE_OVERFLOW_REROUTE = 0, 1
 
 
 class MoeShape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int64), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("d_ff", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
-                ("d_ff_shared", ctypes.c_int32), ("routing", ctypes.c_int32)]
+                ("d_ff_shared", ctypes.c_int32), ("routing", ctypes.c_int32), ("gates", ctypes.c_int32),
+                ("overflow", ctypes.c_int32)]
 
 
 class MoeShared(ctypes.Structure):

@@ -46,10 +46,15 @@ ROUTINGS = {"token": MOE_ROUTE_TOKEN_CHOICE, "expert": MOE_ROUTE_EXPERT_CHOICE,
             MOE_ROUTE_TOKEN_CHOICE: MOE_ROUTE_TOKEN_CHOICE, MOE_ROUTE_EXPERT_CHOICE: MOE_ROUTE_EXPERT_CHOICE}
 
 
+GATES = {"renorm": 0, "raw": 1, 0: 0, 1: 1}
+OVERFLOWS = {"drop": 0, "reroute": 1, 0: 0, 1: 1}
+
+
 def shape_of(T: int, d: int, E: int, k: int, d_ff: int, dtype: torch.dtype, act, d_ff_shared: int = 0,
-             routing="token") -> MoeShape:
+             routing="token", gates="renorm", overflow="drop") -> MoeShape:
     return MoeShape(T=int(T), d=int(d), E=int(E), k=int(k), d_ff=int(d_ff), dtype=_dtype_code(dtype),
-                    act=ACTS[act], d_ff_shared=int(d_ff_shared), routing=ROUTINGS[routing])
+                    act=ACTS[act], d_ff_shared=int(d_ff_shared), routing=ROUTINGS[routing], gates=GATES[gates],
+                    overflow=OVERFLOWS[overflow])
 
 
 def shared_weights(W1s, W2s, W3s=None, b1s=None, b2s=None) -> MoeShared:
@@ -90,11 +95,12 @@ def get_device_error(ws: torch.Tensor, stream=None) -> int:
 
 
 def route(x: torch.Tensor, W_g: torch.Tensor, k: int, b_g=None, W_noise=None, eps=None,
-          want_logits: bool = False, stats: Optional[torch.Tensor] = None, stream=None):
-    """Router logits + exact top-k + gates.  Returns (idx int32 [T,k], w fp32 [T,k], logits or None)."""
+          want_logits: bool = False, stats: Optional[torch.Tensor] = None, stream=None, gates="renorm"):
+    """Router logits + exact top-k + gates (renormalised, or "raw" routing
+    probabilities).  Returns (idx int32 [T,k], w fp32 [T,k], logits or None)."""
     T, d = x.shape
     E = W_g.shape[1]
-    shape = shape_of(T, d, E, k, 64, x.dtype, MOE_ACT_GELU)
+    shape = shape_of(T, d, E, k, 64, x.dtype, MOE_ACT_GELU, gates=gates)
     idx = torch.empty(T, k, dtype=torch.int32, device=x.device)
     w = torch.empty(T, k, dtype=torch.float32, device=x.device)
     logits = torch.empty(T, E, dtype=torch.float32, device=x.device) if want_logits else None
@@ -247,7 +253,8 @@ class MoELayer:
 
     def __init__(self, W_g, W1, W2, k: int, act, W3=None, b_g=None, W_noise=None, b1=None, b2=None,
                  capacity_factor: Optional[float] = None, C: Optional[int] = None, keep_routing: bool = True,
-                 want_moe: bool = False, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None, routing="token"):
+                 want_moe: bool = False, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None, routing="token",
+                 gates="renorm", overflow="drop"):
         if (capacity_factor is None) == (C is None):
             raise ValueError("give exactly one of capacity_factor and C")
         if (W1s is None) != (W2s is None):
@@ -259,6 +266,7 @@ class MoELayer:
         self.dtype = W1.dtype
         self.Fs = 0 if W1s is None else int(W1s.shape[0])
         self.routing = ROUTINGS[routing]
+        self.gates, self.overflow = GATES[gates], OVERFLOWS[overflow]
         self._shared_t = (W1s, W2s, W3s, b1s, b2s)
         self._shared = shared_weights(W1s, W2s, W3s, b1s, b2s) if W1s is not None else None
         self.capacity_factor, self.C_fixed = capacity_factor, C
@@ -286,7 +294,8 @@ class MoELayer:
         C = self.capacity(T)
         key = (T, C)
         if key not in self._ws:
-            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act, self.Fs, self.routing)
+            shape = shape_of(T, self.d, self.E, self.k, self.F, self.dtype, self.act, self.Fs, self.routing,
+                             self.gates, self.overflow)
             self._ws[key] = new_workspace(shape, C, self.W1.device)
         return self._ws[key]
 
@@ -294,7 +303,8 @@ class MoELayer:
                  stats: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         T = x.shape[0]
         C = self.capacity(T)
-        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act, self.Fs, self.routing)
+        shape = shape_of(T, self.d, self.E, self.k, self.F, x.dtype, self.act, self.Fs, self.routing, self.gates,
+                         self.overflow)
         ws = self.workspace(T)
         dev = x.device
         if out is None:
@@ -370,7 +380,7 @@ def _capture(layer, x, eps, out):
 def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=None, b1=None, b2=None,
             capacity_factor: Optional[float] = None, C: Optional[int] = None, want_moe: bool = False,
             stats: Optional[torch.Tensor] = None, stream=None, W1s=None, W2s=None, W3s=None, b1s=None, b2s=None,
-            routing="token"):
+            routing="token", gates="renorm", overflow="drop"):
     """One-shot whole-layer forward.  Returns (out, routing dict incl. 'moe' when want_moe)."""
     if C is None and capacity_factor is None:
         raise ValueError("give capacity_factor or C")
@@ -378,7 +388,7 @@ def forward(x, W_g, k: int, act, W1, W2, W3=None, b_g=None, W_noise=None, eps=No
         capacity_factor = None
     layer = MoELayer(W_g, W1, W2, k, act, W3=W3, b_g=b_g, W_noise=W_noise, b1=b1, b2=b2,
                      capacity_factor=capacity_factor, C=C, keep_routing=True, want_moe=want_moe,
-                     W1s=W1s, W2s=W2s, W3s=W3s, b1s=b1s, b2s=b2s, routing=routing)
+                     W1s=W1s, W2s=W2s, W3s=W3s, b1s=b1s, b2s=b2s, routing=routing, gates=gates, overflow=overflow)
     out = layer(x, eps=eps, stats=stats, stream=stream)
     return out, layer.last
 

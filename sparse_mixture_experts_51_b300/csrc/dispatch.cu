@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
     int e = my_e[i];
     const long long j = base + static_cast<long long>(i) * NT + tid;
     if (j < total && (e < 0 || e >= E)) {  // an expert id out of range takes no slot
-      record_error(p.err, MOE_ERR_BOUNDS);
+      if (!(p.allow_skip && e == -1)) record_error(p.err, MOE_ERR_BOUNDS);
       e = -1;
     }
     my_e[i] = e;
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
       const int t = static_cast<int>(j - static_cast<long long>(r) * p.T);
       int ps = -1;
       if (my_e[i] >= 0) {
-        const int slot = s_excl[my_e[i]] + my_rank[i];
+        const int slot = (p.base ? __ldg(p.base + my_e[i]) : 0) + s_excl[my_e[i]] + my_rank[i];
         ps = slot < p.C ? slot : -1;
       }
       p.pos[static_cast<long long>(t) * p.k + r] = ps;
@@ -215,7 +215,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
     for (int ex = tid; ex < kMaxExperts; ex += NT) {
       int c = 0;
       if (ex < E) {
-        const int load = s_excl[ex] + s_tot[ex];
+        const int load = (p.base ? __ldg(p.base + ex) : 0) + s_excl[ex] + s_tot[ex];
         c = load < p.C ? load : p.C;
         drop += static_cast<unsigned long long>(load - c);
         p.counts[ex] = c;
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
       const int t = j - r * p.T;
       e = __ldg(p.idx + t * p.k + r);
       if (e < 0 || e >= E) {  // an expert id out of range takes no slot
-        record_error(p.err, MOE_ERR_BOUNDS);
+        if (!(p.allow_skip && e == -1)) record_error(p.err, MOE_ERR_BOUNDS);
         e = -1;
       }
     }
@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
       int ps = -1;
       const int e = (my_er[i] & 0xff) - 1;
       if (e >= 0) {
-        const int slot = s_hist[(i * SNW + warp) * E + e] + (my_er[i] >> 8);
+        const int slot = (p.base ? __ldg(p.base + e) : 0) + s_hist[(i * SNW + warp) * E + e] + (my_er[i] >> 8);
         ps = slot < p.C ? slot : -1;
       }
       p.pos[t * p.k + r] = ps;
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
   // ---- counts, segment offsets, drop count
   unsigned long long drop = 0;
   for (int ex = tid; ex < E; ex += SNT) {
-    const int load = s_tot[ex];
+    const int load = (p.base ? __ldg(p.base + ex) : 0) + s_tot[ex];
     const int c = load < p.C ? load : p.C;
     drop += static_cast<unsigned long long>(load - c);
     p.counts[ex] = c;
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int ex = lane * 4 + q;
-      v[q] = ex < E ? min(s_tot[ex], p.C) : 0;
+      v[q] = ex < E ? min((p.base ? __ldg(p.base + ex) : 0) + s_tot[ex], p.C) : 0;
       run += v[q];
     }
     int incl = run;
@@ -399,6 +399,51 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
     }
   }
   pdl_trigger();
+}
+
+// Overflow re-routing, requests: the first dropped assignment (lowest rank)
+// of each token asks for the token's backup expert; everything else asks
+// for nothing (-1).  A thread per token.
+__global__ void __launch_bounds__(256) reroute_requests_kernel(RerouteParams p) {
+  pdl_wait();
+  pdl_trigger();
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= p.T) return;
+  bool asked = false;
+  const int b = __ldg(p.backup + t);
+  for (int r = 0; r < p.k; ++r) {
+    const long long a = t * p.k + r;
+    const bool ask = !asked && b >= 0 && p.pos[a] < 0;
+    p.req[a] = ask ? b : -1;
+    asked |= p.pos[a] < 0;
+  }
+}
+
+// Merge of the second pass: a request that got a slot moves its assignment
+// to the backup; the assignments still without a slot are counted.
+__global__ void __launch_bounds__(256) reroute_merge_kernel(RerouteParams p) {
+  __shared__ int s_cnt;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const long long a = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  bool lost = false;
+  if (a < static_cast<long long>(p.T) * p.k) {
+    int ps = p.pos[a];
+    const int q = __ldg(p.pos2 + a);
+    if (ps < 0 && p.req[a] >= 0 && q >= 0) {
+      p.idx[a] = p.req[a];
+      p.pos[a] = q;
+      ps = q;
+    }
+    lost = ps < 0;
+  }
+  const unsigned m = __ballot_sync(0xffffffffu, lost);
+  if ((threadIdx.x & 31) == 0 && m) atomicAdd(&s_cnt, __popc(m));
+  __syncthreads();
+  if (threadIdx.x == 0 && s_cnt)
+    atomicAdd(reinterpret_cast<unsigned long long*>(p.dropped), static_cast<unsigned long long>(s_cnt));
 }
 
 // One warp per assignment (t, r): copy token t into its expert-ordered row.
@@ -492,6 +537,18 @@ cudaError_t launch_gather(const GatherParams& p, cudaStream_t st) {
                      reinterpret_cast<uintptr_t>(p.x_perm) % 16 == 0;
   if (vec16) return launch_pdl(gather_kernel<16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, p.rows_alloc);
   return launch_pdl(gather_kernel<4>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, p.rows_alloc);
+}
+
+cudaError_t launch_reroute_requests(const RerouteParams& p, cudaStream_t st) {
+  if (p.T == 0) return cudaSuccess;
+  return launch_pdl(reroute_requests_kernel, dim3(static_cast<unsigned>((p.T + 255) / 256)), dim3(256), 0, st, 1, p);
+}
+
+cudaError_t launch_reroute_merge(const RerouteParams& p, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(p.dropped, 0, sizeof(long long), st);
+  if (e != cudaSuccess || p.T == 0) return e;
+  const long long n = static_cast<long long>(p.T) * p.k;
+  return launch_pdl(reroute_merge_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, st, 1, p);
 }
 
 }  // namespace moe

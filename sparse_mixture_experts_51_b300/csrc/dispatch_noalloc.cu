@@ -79,6 +79,8 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C
       shape->d_ff < 1 || (shape->dtype != MOE_F32 && shape->dtype != MOE_BF16) ||
       (shape->act != MOE_ACT_GELU && shape->act != MOE_ACT_SWIGLU))
     return MOE_ERR_INVALID_ARG;
+  // the plain token-choice dispatch only: no expert choice, no re-routing pass
+  if (shape->routing != MOE_ROUTE_TOKEN_CHOICE || shape->overflow != MOE_OVERFLOW_DROP) return MOE_ERR_INVALID_ARG;
   if (shape->E > kMaxExperts || shape->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   const long long Tk = shape->T * static_cast<long long>(shape->k);
   if (Tk > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array

@@ -67,6 +67,10 @@ struct WsLayout {
   size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
   size_t counts, offsets;    // [E], [E+1] int32
   size_t dropped;            // int64
+  size_t rr_backup;          // [T] int32 (overflow re-routing only, else empty)
+  size_t rr_req, rr_pos2;    // [T,k] int32
+  size_t rr_counts1;         // [E] int32: counts after the first pass
+  size_t rr_dropped2;        // int64
   size_t x_perm;             // [R,d] dtype
   size_t h;                  // [R,F] dtype
   size_t y_perm;             // [R,d] fp32
@@ -103,6 +107,8 @@ struct RouterParams {
   float* logits;
   float* radius;    // [T,E] out or null: a rigorous bound on |logit - exact logit|
   float* lse;       // [T] out or null: log-sum-exp of the token's fp32 logits
+  int32_t* backup;  // [T] out or null: the (k+1)-th ranked expert, exact like the top-k (-1 if k = E)
+  int gate_raw;     // 1: gates are the full-softmax probabilities of the selected experts
   long long* stats;
   int* err;
 };
@@ -123,9 +129,26 @@ struct DispatchParams {
   int* incl;       // [nblk][E]
   int nblk;
   int stall_block;  // testing hook: this tile never publishes its status (-1 = none)
+  const int32_t* base;  // [E] or null: slots already taken in each expert (a second, re-routing pass)
+  int allow_skip;       // 1: an expert id of -1 is no assignment (not an error)
   int* err;
 };
 cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st);
+
+// Overflow re-routing around a second dispatch pass: requests (the first
+// dropped assignment of each token asks for its backup expert), then the
+// merge of the second pass into the tables of the first.
+struct RerouteParams {
+  const int32_t* backup;  // [T]
+  int32_t* idx;           // [T,k] in/out: expert of each assignment (rerouted ones replaced)
+  int32_t* pos;           // [T,k] in/out: slot (rerouted ones filled in)
+  int32_t* req;           // [T,k] out (requests pass) / in (merge pass): backup asked for, or -1
+  const int32_t* pos2;    // [T,k] second-pass slots
+  long long* dropped;     // out (merge): assignments left without an expert
+  int T, k;
+};
+cudaError_t launch_reroute_requests(const RerouteParams& p, cudaStream_t st);
+cudaError_t launch_reroute_merge(const RerouteParams& p, cudaStream_t st);
 
 struct GatherParams {
   const void* x;

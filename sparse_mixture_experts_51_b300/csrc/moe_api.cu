@@ -61,6 +61,12 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.counts = take(sizeof(int32_t) * s.E);
   L.offsets = take(sizeof(int32_t) * (s.E + 1));
   L.dropped = take(sizeof(long long));
+  const bool rr = s.overflow == MOE_OVERFLOW_REROUTE;
+  L.rr_backup = take(rr ? sizeof(int32_t) * static_cast<size_t>(s.T) : 0);
+  L.rr_req = take(rr ? sizeof(int32_t) * Tk : 0);
+  L.rr_pos2 = take(rr ? sizeof(int32_t) * Tk : 0);
+  L.rr_counts1 = take(rr ? sizeof(int32_t) * s.E : 0);
+  L.rr_dropped2 = take(rr ? sizeof(long long) : 0);
   L.x_perm = take(b * static_cast<size_t>(L.rows) * s.d);
   L.h = take(b * static_cast<size_t>(L.rows) * s.d_ff);
   L.y_perm = take(sizeof(float) * static_cast<size_t>(L.rows) * s.d);
@@ -85,6 +91,10 @@ moe_status_t check_shape(const moe_shape_t* s) {
   if (s->routing != MOE_ROUTE_TOKEN_CHOICE && s->routing != MOE_ROUTE_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
   if (s->routing == MOE_ROUTE_EXPERT_CHOICE && s->T * static_cast<long long>(s->E) >= (1LL << 31))
     return MOE_ERR_UNSUPPORTED;
+  if (s->gates != MOE_GATES_RENORM && s->gates != MOE_GATES_RAW) return MOE_ERR_INVALID_ARG;
+  if (s->overflow != MOE_OVERFLOW_DROP && s->overflow != MOE_OVERFLOW_REROUTE) return MOE_ERR_INVALID_ARG;
+  if (s->routing == MOE_ROUTE_EXPERT_CHOICE && (s->gates != MOE_GATES_RENORM || s->overflow != MOE_OVERFLOW_DROP))
+    return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -150,9 +160,36 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g
   p.idx = idx;
   p.w = w;
   p.logits = logits;
+  p.gate_raw = shape->gates == MOE_GATES_RAW ? 1 : 0;
   p.stats = reinterpret_cast<long long*>(stats);
   p.err = nullptr;
   return cuda_status(launch_router(p, shape->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+// The token-choice router of the whole layer: moe_route, plus the backup
+// expert of each token when overflow re-routing is on.
+static moe_status_t route_impl(const moe_shape_t* shape, const void* x, const float* W_g, const float* b_g,
+                               const float* W_noise, const float* eps, int32_t* idx, float* w, float* logits,
+                               int64_t* stats, int32_t* backup, int* err, cudaStream_t st) {
+  if (shape->T == 0) return MOE_OK;
+  RouterParams p{};
+  p.x = x;
+  p.W_g = W_g;
+  p.b_g = b_g;
+  p.W_n = W_noise;
+  p.eps = eps;
+  p.T = static_cast<int>(shape->T);
+  p.d = shape->d;
+  p.E = shape->E;
+  p.k = shape->k;
+  p.idx = idx;
+  p.w = w;
+  p.logits = logits;
+  p.backup = backup;
+  p.gate_raw = shape->gates == MOE_GATES_RAW ? 1 : 0;
+  p.stats = reinterpret_cast<long long*>(stats);
+  p.err = err;
+  return cuda_status(launch_router(p, shape->dtype, st));
 }
 
 // Expert-choice routing: the router in its no-top-k mode (logits, radii,
@@ -213,10 +250,12 @@ __global__ void ec_gates_kernel(const int32_t* sel, const float* gate_te, int E,
   gates[row] = gate_te[static_cast<long long>(sel[row]) * E + e];
 }
 
-static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int32_t* idx, const void* x,
+static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, int32_t* idx, const void* x,
                                   int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
                                   void* x_perm, int32_t* row_token, void* ws, const WsLayout& L,
-                                  cudaStream_t st, int stall_block = -1, int32_t* row_of = nullptr) {
+                                  cudaStream_t st, int stall_block = -1, int32_t* row_of = nullptr,
+                                  const int32_t* backup = nullptr) {
+  const bool rr = backup != nullptr;
   DispatchParams dp{};
   dp.idx = idx;
   dp.T = static_cast<int>(shape->T);
@@ -234,8 +273,34 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, const int
   dp.nblk = L.nblk_dispatch;
   dp.stall_block = stall_block;
   dp.err = at<int>(ws, L.err);
+  if (rr) {
+    // first pass into scratch counts / drop count; the second pass writes the real ones
+    dp.counts = at<int32_t>(ws, L.rr_counts1);
+    dp.dropped = at<long long>(ws, L.rr_dropped2);
+  }
   cudaError_t e = launch_dispatch(dp, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (rr) {
+    RerouteParams rp{};
+    rp.backup = backup;
+    rp.idx = idx;
+    rp.pos = pos;
+    rp.req = at<int32_t>(ws, L.rr_req);
+    rp.pos2 = at<int32_t>(ws, L.rr_pos2);
+    rp.dropped = reinterpret_cast<long long*>(dropped);
+    rp.T = static_cast<int>(shape->T);
+    rp.k = shape->k;
+    if (launch_reroute_requests(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+    DispatchParams d2 = dp;
+    d2.idx = rp.req;
+    d2.pos = at<int32_t>(ws, L.rr_pos2);
+    d2.counts = counts;
+    d2.dropped = at<long long>(ws, L.rr_dropped2);
+    d2.base = at<int32_t>(ws, L.rr_counts1);
+    d2.allow_skip = 1;
+    if (launch_dispatch(d2, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_reroute_merge(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
   GatherParams gp{};
   gp.x = x;
   gp.idx = idx;
@@ -294,14 +359,15 @@ moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int32_t* id
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;  // token-choice tables
+  if (shape->overflow != MOE_OVERFLOW_DROP) return MOE_ERR_INVALID_ARG;     // re-routing: moe_forward only
   if (C < 0) return MOE_ERR_INVALID_ARG;
   if (counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*shape, C);
   if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
-  return dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, x_perm, row_token, ws, L,
-                       static_cast<cudaStream_t>(stream));
+  return dispatch_impl(shape, C, const_cast<int32_t*>(idx), x, pos, counts, offsets, dropped, x_perm, row_token,
+                       ws, L, static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_testing_dispatch_stalled(const moe_shape_t* shape, int32_t C, const int32_t* idx,
@@ -311,14 +377,15 @@ moe_status_t moe_testing_dispatch_stalled(const moe_shape_t* shape, int32_t C, c
   moe_status_t st = check_shape(shape);
   if (st != MOE_OK) return st;
   if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;  // token-choice tables
+  if (shape->overflow != MOE_OVERFLOW_DROP) return MOE_ERR_INVALID_ARG;     // re-routing: moe_forward only
   if (C < 0 || counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
   if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*shape, C);
   if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
   if (stalled_tile < 0 || stalled_tile >= L.nblk_dispatch) return MOE_ERR_INVALID_ARG;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
-  return dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, x_perm, nullptr, ws, L,
-                       static_cast<cudaStream_t>(stream), stalled_tile);
+  return dispatch_impl(shape, C, const_cast<int32_t*>(idx), x, pos, counts, offsets, dropped, x_perm, nullptr, ws,
+                       L, static_cast<cudaStream_t>(stream), stalled_tile);
 }
 
 static moe_status_t ffn_impl(const moe_shape_t* shape, const void* x_perm, const int32_t* offsets, const void* W1,
@@ -532,10 +599,12 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     gate = ep.gate_te;
     cshape.k = shape->E;
   } else {
-    if ((st = moe_route(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, stream)) != MOE_OK) return st;
+    int32_t* backup = shape->overflow == MOE_OVERFLOW_REROUTE ? at<int32_t>(ws, L.rr_backup) : nullptr;
+    if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s)) != MOE_OK)
+      return st;
     if ((st = mark(1)) != MOE_OK) return st;
     if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
-                            s, -1, row_of)) != MOE_OK)
+                            s, -1, row_of, backup)) != MOE_OK)
       return st;
   }
   if ((st = mark(2)) != MOE_OK) return st;

@@ -139,6 +139,8 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
                                            const float (&z)[SLOTS], float nx, const float* cn2, float gam,
                                            WCol wcol, int& n_recomputed, int& n_near) {
   const int E = p.E, k = p.k, d = p.d;
+  // ranks settled exactly: the top k, and the (k+1)-th too when the backup is asked for
+  const int kr = (p.backup != nullptr && k < E) ? k + 1 : k;
   const bool noisy = p.W_n != nullptr;
   float H[SLOTS], B[SLOTS];
 #pragma unroll
@@ -192,7 +194,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
   int trank[SLOTS];
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) trank[s] = -1;
-  for (int r = 0; r < k; ++r) {
+  for (int r = 0; r < kr; ++r) {
     float bv = -INFINITY, bb = 0.f;
     int be = 0x7fffffff;
 #pragma unroll
@@ -230,7 +232,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
   // rank r is exact when its lower end lies above the upper end of every
   // expert ranked below it: a suffix maximum of the upper ends over lanes
   // (lane k carries the experts left out).
-  float sm = lane < k ? my_h + my_b : (lane == k ? restU : -INFINITY);
+  float sm = lane < kr ? my_h + my_b : (lane == kr ? restU : -INFINITY);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float n2 = __shfl_down_sync(0xffffffffu, sm, o);
@@ -238,13 +240,14 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
   }
   const float below = __shfl_down_sync(0xffffffffu, sm, 1);
   const float lo = my_h - my_b;
+  const float h_k = __shfl_sync(0xffffffffu, my_h, k & 31);  // the (k+1)-th value when it was ranked
   bool safe = true, near = false;
-  if (lane < k) {
+  if (lane < kr) {
     safe = lo > below && lo > -INFINITY && my_b < INFINITY;
-    if (lane == k - 1 && k < E) near = my_h - restH < 1e-4f;
+    if (lane == k - 1 && k < E) near = my_h - (kr > k ? h_k : restH) < 1e-4f;
   }
   if (__any_sync(0xffffffffu, near)) ++n_near;
-  const unsigned unsafe = __ballot_sync(0xffffffffu, !safe) & ((1u << k) - 1u);
+  const unsigned unsafe = __ballot_sync(0xffffffffu, !safe) & ((1u << kr) - 1u);
 
   if (unsafe != 0u) {
     // ranks [0, p0) are exact; re-evaluate in fp64 the experts that may hold
@@ -252,7 +255,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
     // upper end reaches the lowest of their lower ends
     ++n_recomputed;
     const int p0 = __ffs(unsafe) - 1;
-    float L = (lane >= p0 && lane < k) ? lo : INFINITY;
+    float L = (lane >= p0 && lane < kr) ? lo : INFINITY;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L = fminf(L, __shfl_xor_sync(0xffffffffu, L, o));
     const TX* xrow = static_cast<const TX*>(p.x) + t * d;
@@ -303,7 +306,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
     bool used[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) used[s] = false;
-    for (int r = p0; r < k; ++r) {
+    for (int r = p0; r < kr; ++r) {
       double bv = -INFINITY;
       int be = 0x7fffffff;
 #pragma unroll
@@ -325,15 +328,24 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
     }
   }
 
-  // gates: softmax over the selected logits, shifted by the largest, summed in rank order
+  // gates: softmax over the selected logits, shifted by the largest, summed in
+  // rank order; raw gates divide by the sum over every expert instead
   const float top = __shfl_sync(0xffffffffu, my_h, 0);
   const float ex = lane < k ? expf(my_h - top) : 0.f;
   float den = 0.f;
-  for (int r = 0; r < k; ++r) den += __shfl_sync(0xffffffffu, ex, r);
+  if (p.gate_raw) {
+    float all = 0.f;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) all += (lane + 32 * s < E && H[s] > -INFINITY) ? expf(H[s] - top) : 0.f;
+    den = warp_sum(all);
+  } else {
+    for (int r = 0; r < k; ++r) den += __shfl_sync(0xffffffffu, ex, r);
+  }
   if (lane < k) {
     p.idx[t * k + lane] = my_e;
     p.w[t * k + lane] = ex / den;
   }
+  if (p.backup != nullptr && lane == (kr > k ? k : 0)) p.backup[t] = kr > k ? my_e : -1;
 }
 
 __device__ __forceinline__ void flush_stats(const RouterParams& p, int* cnt, int lane, int n_recomputed, int n_near) {

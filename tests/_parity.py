@@ -44,13 +44,13 @@ def shared_args(g: dict) -> dict:
     return dict(W1s=sw["W1s"], W2s=sw["W2s"], W3s=sw["W3s"], b1s=sw["b1s"], b2s=b2)
 
 
-def gpu_forward(w: W.Workload, g: dict, C=None, want_moe=True):
+def gpu_forward(w: W.Workload, g: dict, C=None, want_moe=True, gates="renorm", overflow="drop"):
     stats = torch.zeros(2, dtype=torch.int64, device="cuda")
     act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
     out, r = api.forward(g["x"], g["W_g"], w.k, act, g["W1"], g["W2"], W3=g["W3"], b_g=g["b_g"],
                          W_noise=g["W_noise"], eps=g["eps"], b1=g["b1"], b2=g["b2"],
                          capacity_factor=None if C is not None else w.capacity_factor, C=C,
-                         want_moe=want_moe, stats=stats, **shared_args(g))
+                         want_moe=want_moe, stats=stats, gates=gates, overflow=overflow, **shared_args(g))
     torch.cuda.synchronize()
     res = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in r.items()}
     res["out"] = out.cpu()
@@ -67,7 +67,8 @@ def oracle_shared(inp: dict):
                 b2s=f(inp.get("b2s")))
 
 
-def oracle_forward(w: W.Workload, inp: dict, C=None, tokens=None, idx_override=None):
+def oracle_forward(w: W.Workload, inp: dict, C=None, tokens=None, idx_override=None, gates="renorm",
+                   overflow="drop"):
     f = W.as_f64_numpy
     return O.forward(f(inp["x"]), f(inp["W_g"]), w.k, w.act, F64Experts(inp["W1"]), F64Experts(inp["W2"]),
                      W3=None if inp["W3"] is None else F64Experts(inp["W3"]),
@@ -75,7 +76,7 @@ def oracle_forward(w: W.Workload, inp: dict, C=None, tokens=None, idx_override=N
                      b2=None if inp["b2"] is None else F64Experts(inp["b2"]),
                      b_g=f(inp["b_g"]), W_noise=f(inp["W_noise"]), eps=f(inp["eps"]),
                      capacity_factor=w.capacity_factor if C is None else None, C=C, tokens=tokens,
-                     idx_override=idx_override, shared=oracle_shared(inp))
+                     idx_override=idx_override, shared=oracle_shared(inp), gate_mode=gates, overflow=overflow)
 
 
 def tolerance(w: W.Workload) -> float:

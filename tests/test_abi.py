@@ -234,3 +234,18 @@ def test_expert_choice_argument_errors(lib):
     args = [f, f, None, None, None, f, None, f, None, None, None, f, None, f, None, None, None, None, None, None,
             None]
     assert lib.moe_forward(ctypes.byref(ec), 1.25, -1, *args, f, n, None) == INVALID
+
+
+@no_gpu
+def test_overflow_and_gate_option_errors(lib):
+    f = P(FAKE)
+    assert _ws(lib, _shape(gates=2), 40)[0] == INVALID
+    assert _ws(lib, _shape(overflow=2), 40)[0] == INVALID
+    assert _ws(lib, _shape(routing=1, gates=1), 40)[0] == INVALID      # expert choice: gates are p by definition
+    assert _ws(lib, _shape(routing=1, overflow=1), 40)[0] == INVALID   # expert choice: nothing overflows
+    rr = _shape(overflow=1)
+    st, n = _ws(lib, rr, 40)
+    assert st == OK and n > _ws(lib, _shape(), 40)[1]  # room for the second dispatch pass
+    # re-routing runs only inside moe_forward
+    assert lib.moe_dispatch(ctypes.byref(rr), 40, f, f, f, f, f, f, f, None, f, n, None) == INVALID
+    assert lib.moe_dispatch_noalloc(ctypes.byref(rr), 40, f, f, f, f, f, f, f, None, None, None) == INVALID
