@@ -501,18 +501,14 @@ cudaError_t launch_single(const DispatchParams& p, cudaStream_t st) {
 cudaError_t launch_dispatch(const DispatchParams& p, cudaStream_t st) {
   cudaError_t e = cudaSuccess;
   const long long Tk = static_cast<long long>(p.T) * p.k;
-  // one CTA for up to 8192 assignments (8 per thread: more would spill) when
-  // its histogram (items per thread x 32 warps x E ints) fits in 96 KB
+  // one CTA for up to 2048 assignments when its histogram (items per thread
+  // x 32 warps x E ints) fits in 96 KB; measured on B300 it wins at 768
+  // assignments (1.5 us) and loses to the tiled kernel at 8192 (2.5 us)
   int items = 1;
   while (static_cast<long long>(items) * SNT < Tk) items <<= 1;
   // (the testing hook that stalls a tile needs the tiled kernel)
-  if (p.stall_block < 0 && items <= 8 && static_cast<long long>(items) * SNW * p.E * 4 <= 96 * 1024) {
-    switch (items) {
-      case 1: return launch_single<1>(p, st);
-      case 2: return launch_single<2>(p, st);
-      case 4: return launch_single<4>(p, st);
-      default: return launch_single<8>(p, st);
-    }
+  if (p.stall_block < 0 && items <= 2 && static_cast<long long>(items) * SNW * p.E * 4 <= 96 * 1024) {
+    return items == 1 ? launch_single<1>(p, st) : launch_single<2>(p, st);
   }
   if (p.clear_ctrl && (e = cudaMemsetAsync(p.ctrl, 0, sizeof(int) * (2 + p.nblk), st)) != cudaSuccess) return e;
   if (dispatch_items(Tk) == kDispatchItemsSmall) {

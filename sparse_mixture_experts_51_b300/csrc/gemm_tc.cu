@@ -285,60 +285,63 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
         for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
-          float gv[32], uv[32];
-          tmem_ld32(tbase + c * 32, gv);
-          tmem_ld32(tbase + 128 + c * 32, uv);
+          // gate and up columns in flight together, one wait
+          uint32_t gr[32], ur[32];
+          tmem_ld32_issue(tbase + c * 32, gr);
+          tmem_ld32_issue(tbase + 128 + c * 32, ur);
+          tmem_wait_ld(gr, ur);
           const int col = ti.n0 + c * 32;
           if (row_ok && col < g.N_out) {
             uint4 pk[4];
             __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              h2[i] = __floats2bfloat162_rn(silu_f(gv[2 * i]) * uv[2 * i], silu_f(gv[2 * i + 1]) * uv[2 * i + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
-          }
-        }
-      } else if constexpr (MODE == MODE_GELU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
-#pragma unroll 1
-        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-          const int col = ti.n0 + c * 32;
-          if (row_ok && col < g.N_out) {
-            const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
-            uint4 pk[4];
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float a0 = v[2 * i], a1 = v[2 * i + 1];
-              if (bias) { a0 += bias[2 * i]; a1 += bias[2 * i + 1]; }
-              h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
-            }
+              h2[i] = __floats2bfloat162_rn(silu_f(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
+                                            silu_f(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
             uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i) dst[i] = pk[i];
           }
         }
       } else {
-        float* out = static_cast<float*>(g.out);
-#pragma unroll 1
-        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
+        // two 32-column chunks in flight per wait
+        auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
           const int col = ti.n0 + c * 32;
-          if (row_ok && col < g.N_out) {
-            const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
+          if (!(row_ok && col < g.N_out)) return;
+          const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
+          if constexpr (MODE == MODE_GELU) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
+            uint4 pk[4];
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
+              if (bias) { a0 += bias[2 * i]; a1 += bias[2 * i + 1]; }
+              h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+          } else {
+            float* out = static_cast<float*>(g.out);
             float4* dst = reinterpret_cast<float4*>(out + row * g.out_ld + col);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float4 o = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+              float4 o = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
               if (bias) { o.x += bias[4 * i]; o.y += bias[4 * i + 1]; o.z += bias[4 * i + 2]; o.w += bias[4 * i + 3]; }
               dst[i] = o;
             }
           }
+        };
+#pragma unroll 1
+        for (int c = cfirst; c < BN_OUT / 32; c += 2 * CSTEP) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_issue(tbase + c * 32, r0);
+          tmem_ld32_issue(tbase + (c + CSTEP) * 32, r1);
+          tmem_wait_ld(r0, r1);
+          store_chunk(c, r0);
+          store_chunk(c + CSTEP, r1);
         }
       }
       tc_fence_before();

@@ -46,7 +46,7 @@ constexpr int WT = 384;   // threads per CTA, warp kernel
 // ================================================================ warp kernel
 // Shared memory: Wt [NC][ldw] fp32 (column c of [W_g | W_noise] as a row,
 // zero rows for c >= nc), red [WT/32][40] per-warp reduced logits and token
-// norms, cn2 [NC],
+// norms, cn2 [NC] (column norms of the combined weight),
 // cnt [2].  ldw = d rounded up to 128, plus 4 (conflict-free transposed store).
 struct WarpPlan {
   int nc;       // logit columns
@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
     float s2 = 0.f;
     for (int j = lane; j < d; j += 32) s2 = fmaf(Wt[c * ldw + j], Wt[c * ldw + j], s2);
     s2 = warp_sum(s2);
-    if (lane == 0) cn2[c] = s2;
+    if (lane == 0) cn2[c] = sqrtf(s2);  // the column norm itself: every token's bound uses it
   }
   __syncthreads();
 
@@ -105,6 +105,11 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
 
   for (long long grp = static_cast<long long>(blockIdx.x) * (WT / 32) + warp; grp < q.ngroups_tok; grp += wstride) {
     const long long tbase = grp * TW;
+    // the noise of this batch's tokens, requested before the contraction so
+    // its memory latency is hidden behind it
+    float ep[TW][1];
+#pragma unroll
+    for (int u = 0; u < TW; ++u) load_eps<1>(p, tbase + u, lane, ep[u]);
     float acc[TW][NC], sq[TW];
 #pragma unroll
     for (int u = 0; u < TW; ++u) {
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
       g[0] = lane < E ? myred[u * NC + lane] : 0.f;
       z[0] = (p.W_n != nullptr && lane < E) ? myred[u * NC + E + lane] : 0.f;
       auto wcol = [&](int c, int j) { return *reinterpret_cast<const float4*>(&Wt[c * ldw + j]); };
-      rank_token<TX, 1>(p, t, lane, g, z, sqrtf(myred[32 + u]), cn2, gam, wcol, n_recomputed, n_near);
+      rank_token<TX, 1>(p, t, lane, g, z, ep[u], sqrtf(myred[32 + u]), cn2, gam, wcol, n_recomputed, n_near);
     }
     __syncwarp();
   }

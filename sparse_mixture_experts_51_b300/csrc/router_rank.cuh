@@ -127,17 +127,29 @@ __device__ __forceinline__ void cp_async4(float* dst, const float* src, bool val
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
+// eps[t, lane + 32 s] for the noisy logits (0 without noise or past the end).
+template <int SLOTS>
+__device__ __forceinline__ void load_eps(const RouterParams& p, long long t, int lane, float (&ep)[SLOTS]) {
+#pragma unroll
+  for (int s = 0; s < SLOTS; ++s) {
+    const int e = lane + 32 * s;
+    ep[s] = (p.eps != nullptr && p.W_n != nullptr && t < p.T && e < p.E) ? __ldg(p.eps + t * p.E + e) : 0.f;
+  }
+}
+
 // ---------------------------------------------------------------- ranking
 // One warp ranks token t.  Lane e + 32 s holds, in g[s] (and z[s] with the
 // noise projection), the fp32 contraction of expert e = lane + 32 s, whose
-// rounding error is at most gam * nx * ||W column|| (cn2: squared column
-// norms of the combined [W_g | W_noise], nc entries).  Writes idx/w (and the
+// rounding error is at most gam * nx * ||W column|| (cn: column norms of the
+// combined [W_g | W_noise], nc entries).  Writes idx/w (and the
 // logits when asked); n_recomputed / n_near count settled-in-fp64 tokens and
 // near ties (warp-uniform).
+// ep[s] is eps[t, lane + 32 s] (loaded early by the caller; unused without noise).
 template <typename TX, int SLOTS, typename WCol>
 __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, int lane, const float (&g)[SLOTS],
-                                           const float (&z)[SLOTS], float nx, const float* cn2, float gam,
-                                           WCol wcol, int& n_recomputed, int& n_near) {
+                                           const float (&z)[SLOTS], const float (&ep_in)[SLOTS], float nx,
+                                           const float* cn, float gam, WCol wcol, int& n_recomputed,
+                                           int& n_near) {
   const int E = p.E, k = p.k, d = p.d;
   // ranks settled exactly: the top k, and the (k+1)-th too when the backup is asked for
   const int kr = (p.backup != nullptr && k < E) ? k + 1 : k;
@@ -152,14 +164,14 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
       const float b = p.b_g ? __ldg(p.b_g + e) : 0.f;
       const float gb = g[s] + b;
       float h = gb, bound;
-      const float cg2 = sqrtf(cn2[e]);
+      const float cg2 = cn[e];
       if (noisy) {
-        const float ep = __ldg(p.eps + t * E + e);
+        const float ep = ep_in[s];
         const float sp = softplus_f32(z[s]);
         const float ns = ep * sp;
         h = gb + ns;
-        const float cn = sqrtf(cn2[E + e]);
-        bound = gam * nx * (cg2 + fabsf(ep) * cn) + fabsf(ep) * (4e-7f + 3e-7f * sp) +
+        const float cnz = cn[E + e];
+        bound = gam * nx * (cg2 + fabsf(ep) * cnz) + fabsf(ep) * (4e-7f + 3e-7f * sp) +
                 4.f * kU * (fabsf(g[s]) + fabsf(b) + fabsf(ns) + fabsf(h));
       } else {
         bound = gam * nx * cg2 + 4.f * kU * (fabsf(g[s]) + fabsf(b) + fabsf(h));

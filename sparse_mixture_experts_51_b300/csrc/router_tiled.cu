@@ -76,12 +76,13 @@ struct Tile {
 __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
 
-template <typename TX, int CQ, int TM>
+// SL: 32-expert slots a lane holds while ranking (E <= 32 * SL).
+template <typename TX, int CQ, int TM, int SL>
 __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, TiledPlan q) {
   using G = Tile<TX, CQ, TM>;
   constexpr int NCP = G::NCP, TB = G::TB, XS_LD = G::XS_LD, VEC = G::VEC, VPT = G::VPT, RS = G::RS;
   constexpr int NV = G::NV;
-  constexpr int SLOTS = kMaxExperts / 32;
+  constexpr int SLOTS = SL;
   extern __shared__ __align__(16) uint8_t smem[];
   float* xt = reinterpret_cast<float*>(smem);                  // [2][DK][XS_LD]
   float* wr = reinterpret_cast<float*>(smem + G::OFF_WR);      // [STAGES][DK][NCP]
@@ -219,13 +220,18 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
   }
   cp_async_wait_all();
   pdl_trigger();
+  // the noise of this warp's first token to rank: requested now, used after
+  // the cluster-wide reduction below
+  const int tl_first = rank * (RT / 32) + warp, tl_step = KS * (RT / 32);
+  float ep_cur[SLOTS];
+  load_eps<SLOTS>(p, t0 + tl_first, lane, ep_cur);
   __syncthreads();  // the slice buffers are dead: the partial-logit tile may alias them
 
   // -------- park this CTA's partial logits and norms in shared memory
   float* Lt = reinterpret_cast<float*>(smem);                   // [TB][LT_LD]
   float* xsq = reinterpret_cast<float*>(smem + G::OFF_XSQ);     // [TB]   partial ||x_t||^2
   float* cn2p = reinterpret_cast<float*>(smem + G::OFF_CN2P);   // [NCP]  partial column sums of W^2
-  float* cn2f = reinterpret_cast<float*>(smem + G::OFF_CN2F);   // [NCP]  full column sums (this CTA)
+  float* cn2f = reinterpret_cast<float*>(smem + G::OFF_CN2F);   // [NCP]  full column norms (not squared)
   float* wq = reinterpret_cast<float*>(smem + G::OFF_WQ);       // [RT]   per-thread W^2 partials
   float* vsq = reinterpret_cast<float*>(smem + G::OFF_VSQ);     // [NV*RT] per-chunk x^2 partials
   int* cnt = reinterpret_cast<int*>(smem + G::OFF_CNT);
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
 #pragma unroll
     for (int r2 = 0; r2 < kMaxCluster; ++r2)
       if (r2 < KS) s2 += part[r2];
-    cn2f[c] = s2;
+    cn2f[c] = sqrtf(s2);  // the column norm itself: every token's bound uses it
   }
   __syncthreads();
 
@@ -273,46 +279,46 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
     return make_float4(__ldg(W + r0), __ldg(W + r0 + E), __ldg(W + r0 + 2 * E), __ldg(W + r0 + 3 * E));
   };
 
-  for (int tl = rank * (RT / 32) + warp; tl < TB; tl += KS * (RT / 32)) {
+  for (int tl = tl_first; tl < TB; tl += tl_step) {
     const long long t = t0 + tl;
     if (t >= p.T) break;
+    // the next token's noise, in flight while this token is ranked
+    float ep_next[SLOTS];
+    load_eps<SLOTS>(p, tl + tl_step < TB ? t + tl_step : p.T, lane, ep_next);
+    // the KS partial tiles summed in rank order (KS = 1: this CTA's own tile)
     float g[SLOTS], z[SLOTS];
     float nx2 = 0.f;
-    {
-      float part[kMaxCluster];
 #pragma unroll
-      for (int r2 = 0; r2 < kMaxCluster; ++r2) part[r2] = r2 < KS ? *cluster.map_shared_rank(xsq + tl, r2) : 0.f;
+    for (int s = 0; s < SLOTS; ++s) { g[s] = 0.f; z[s] = 0.f; }
+    if (KS == 1) {
+      nx2 = xsq[tl];
+      const float* Lr = Lt + tl * G::LT_LD;
 #pragma unroll
-      for (int r2 = 0; r2 < kMaxCluster; ++r2)
-        if (r2 < KS) nx2 += part[r2];
-    }
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-      const int e = lane + 32 * s;
-      g[s] = 0.f;
-      z[s] = 0.f;
-      if (e < E) {
-        float pg[kMaxCluster], pz[kMaxCluster];
-#pragma unroll
-        for (int r2 = 0; r2 < kMaxCluster; ++r2) {
-          pg[r2] = 0.f;
-          pz[r2] = 0.f;
-          if (r2 < KS) {
-            const float* Lr = cluster.map_shared_rank(Lt + tl * G::LT_LD, r2);
-            pg[r2] = Lr[e];
-            if (noisy) pz[r2] = Lr[E + e];
-          }
+      for (int s = 0; s < SLOTS; ++s) {
+        const int e = lane + 32 * s;
+        if (e < E) {
+          g[s] = Lr[e];
+          if (noisy) z[s] = Lr[E + e];
         }
+      }
+    } else {
+#pragma unroll 4
+      for (int r2 = 0; r2 < KS; ++r2) {
+        nx2 += *cluster.map_shared_rank(xsq + tl, r2);
+        const float* Lr = cluster.map_shared_rank(Lt + tl * G::LT_LD, r2);
 #pragma unroll
-        for (int r2 = 0; r2 < kMaxCluster; ++r2) {
-          if (r2 < KS) {
-            g[s] += pg[r2];
-            z[s] += pz[r2];
+        for (int s = 0; s < SLOTS; ++s) {
+          const int e = lane + 32 * s;
+          if (e < E) {
+            g[s] += Lr[e];
+            if (noisy) z[s] += Lr[E + e];
           }
         }
       }
     }
-    rank_token<TX, SLOTS>(p, t, lane, g, z, sqrtf(nx2), cn2f, gam, wcol, n_recomputed, n_near);
+    rank_token<TX, SLOTS>(p, t, lane, g, z, ep_cur, sqrtf(nx2), cn2f, gam, wcol, n_recomputed, n_near);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) ep_cur[s] = ep_next[s];
   }
 
   if (p.stats) flush_stats(p, cnt, lane, n_recomputed, n_near);
@@ -326,10 +332,16 @@ int pow2_at_least(int v) {
   return r;
 }
 
-template <typename TX, int CQ, int TM>
-cudaError_t launch_one(const RouterParams& p, const TiledPlan& q, long long tiles, cudaStream_t st) {
+// expert slots per lane: the logit columns bound E (nc = E, or 2E with noise)
+template <int CQ>
+constexpr int slots_for(bool noisy) {
+  return CQ <= 8 ? 1 : (CQ == 16 ? 2 : (CQ == 32 ? (noisy ? 2 : 4) : 4));
+}
+
+template <typename TX, int CQ, int TM, int SL>
+cudaError_t launch_one_sl(const RouterParams& p, const TiledPlan& q, long long tiles, cudaStream_t st) {
   using G = Tile<TX, CQ, TM>;
-  auto kern = router_tiled_kernel<TX, CQ, TM>;
+  auto kern = router_tiled_kernel<TX, CQ, TM, SL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
   if (e != cudaSuccess) return e;
   if (q.KS > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
@@ -352,6 +364,13 @@ cudaError_t launch_one(const RouterParams& p, const TiledPlan& q, long long tile
   return cudaLaunchKernelEx(&cfg, kern, p, q);
 }
 
+template <typename TX, int CQ, int TM>
+cudaError_t launch_one(const RouterParams& p, const TiledPlan& q, long long tiles, cudaStream_t st) {
+  const bool noisy = p.W_n != nullptr;
+  if (CQ == 32 && noisy) return launch_one_sl<TX, CQ, TM, slots_for<CQ>(true)>(p, q, tiles, st);
+  return launch_one_sl<TX, CQ, TM, slots_for<CQ>(false)>(p, q, tiles, st);
+}
+
 // Whether a 16-CTA cluster of the largest-footprint 16-CTA plan (TM = 1) can
 // be resident; probed once per device.  Otherwise clusters stay within 8.
 constexpr int kMaxDevices = 64;
@@ -361,7 +380,7 @@ std::once_flag g_cluster_once[kMaxDevices];
 template <typename TX, int CQ>
 int probe_cluster16() {
   using G = Tile<TX, CQ, 1>;
-  auto kern = router_tiled_kernel<TX, CQ, 1>;
+  auto kern = router_tiled_kernel<TX, CQ, 1, slots_for<CQ>(false)>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM) != cudaSuccess) {
     cudaGetLastError();
