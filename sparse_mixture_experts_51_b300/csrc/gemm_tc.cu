@@ -225,7 +225,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t aphase = 0;
       bool ok = true;
       bool any = false;
+      int ecur = 0;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        // a 256-row tile holding at most 128 rows of its expert (the last,
+        // partial tile of a segment) computes only its first M half
+        TileInfo ti;
+        decode(tile, ecur, ti);
+        const int mt_used = (MT == 2 && ti.rows_valid <= BM) ? 1 : MT;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aphase ^ 1u, g.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * C::ACC_COLS);
@@ -239,6 +245,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int kk = 0; kk < BK / 16; ++kk) {
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
+              if (m >= mt_used) break;
               // M tile m: rows 128m.. of the A stage (16 KB apart) into TMEM columns 256m..;
               // step 16 bf16 = 32 bytes along K inside the swizzled 128-byte rows
               const uint64_t da = smem_desc_sw128(sa + static_cast<uint32_t>(m * BM * BK * 2));
@@ -281,7 +288,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                              static_cast<uint32_t>(acc * C::ACC_COLS + msel * 256);
       const bool row_ok = rloc < ti.rows_valid;
       const long long row = static_cast<long long>(ti.row0) + rloc;
-      if constexpr (MODE == MODE_SWIGLU) {
+      // a warp whose 32 rows all lie past the segment reads nothing
+      const bool warp_rows = __any_sync(0xffffffffu, row_ok);
+      if (!warp_rows) {
+      } else if constexpr (MODE == MODE_SWIGLU) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
         for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
