@@ -246,6 +246,32 @@ def cpu_oracle_run(w, budget_s: float):
     return tokens / el, sample, cores, el
 
 
+# ---------------------------------------------------------------- ranks
+# bench.py under torchrun runs one independent replica of the layer per GPU:
+# the path has no exchange step.  These helpers hold the host-side logic of
+# that mode (tested with gloo ranks on the CPU).
+
+def replica_workload(w, rank: int, world: int):
+    """Rank r's replica: the same layer with its own token batch (seed + 1000 r)."""
+    return w.with_(seed=w.seed + 1000 * rank) if world > 1 else w
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value over all ranks (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank_step * steps * world / (max_ms / 1e3)
+
+
 # ---------------------------------------------------------------- arms
 
 def run_reference(a):
@@ -305,9 +331,7 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     lib = _lib.load()
 
-    w = W.WORKLOADS[a.workload]
-    if world > 1:
-        w = w.with_(seed=w.seed + 1000 * rank)  # an independent replica batch per rank
+    w = replica_workload(W.WORKLOADS[a.workload], rank, world)
     inp = W.make_inputs(w)
     g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
     act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
@@ -410,13 +434,8 @@ def run_ours(a):
     if err != 0:
         raise RuntimeError(f"device-side error {err} during the timed region")
 
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    tokens_all = w.T * a.steps * world
-    value = tokens_all / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_throughput(w.T, a.steps, world, total_ms)
 
     # ---------------- roofline of the dominant kernel (first expert GEMM)
     cnt = counts.cpu().tolist()
@@ -473,14 +492,10 @@ def run_ours(a):
         e2e_step()
         evs[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in evs)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs), world, dev)
     h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
     d2h = out_host.numel() * out_host.element_size()
-    e2e = {"value": w.T * n_e2e * world / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    e2e = {"value": job_throughput(w.T, n_e2e, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h}
 
     # ---------------- routing diagnostics + aux loss of the same batch (moe_routing_stats,
