@@ -64,6 +64,7 @@ enum { MODE_GELU = 0, MODE_SWIGLU = 1, MODE_DOWN = 2 };
 struct GemmArgs {
   const int32_t* offsets;  // [E+1] segment starts; null: one dense group of dense_rows rows
   int dense_rows;
+  int a_kwrap;             // > 0: k-block kb of A is read at k-block kb mod a_kwrap (A reused along K)
   int E;
   int N_out;      // output columns
   int N_w;        // weight rows per expert in the B tensor
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           mbar_arrive_expect_tx(fb, STAGE_BYTES);
           const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
           const uint32_t sb = sa + A_BYTES;
-          tma_load_2d(sa, &tmA, fb, kb * BK, ti.row0);
+          tma_load_2d(sa, &tmA, fb, (g.a_kwrap > 0 ? kb % g.a_kwrap : kb) * BK, ti.row0);
           if (MODE == MODE_SWIGLU) {
             tma_load_2d(sb, &tmB, fb, kb * BK, brow);
             tma_load_2d(sb + B_BYTES / 2, &tmB3, fb, kb * BK, brow);
@@ -414,6 +415,37 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtens
 }
 
 }  // namespace
+
+// out[r, n] = sum over k < K of A[r, k mod Ka] * B[n, k], fp32 (dense, one group):
+// A [rows, Ka] bf16, B [N, K] bf16, K a multiple of Ka, Ka a multiple of 64.
+cudaError_t launch_dense_wrapped_gemm(const void* A, long long rows, int Ka, const void* B, int N, int K, float* out,
+                                      int* err, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int MT = rows > 4LL * BM ? 2 : 1;
+  CUtensorMap mA, mB;
+  if ((e = make_map(&mA, A, rows, Ka, BM * MT)) != cudaSuccess) return e;
+  if ((e = make_map(&mB, B, N, K, BN)) != cudaSuccess) return e;
+  GemmArgs g{};
+  g.offsets = nullptr;
+  g.dense_rows = static_cast<int>(rows);
+  g.a_kwrap = Ka / BK;
+  g.E = 1;
+  g.N_out = N;
+  g.N_w = N;
+  g.K = K;
+  g.n_tiles = (N + BN - 1) / BN;
+  g.out = out;
+  g.out_ld = N;
+  g.bias = nullptr;
+  g.err = err;
+  return MT == 2 ? launch_mode<MODE_DOWN, 2>(mA, mB, mB, g, rows, sms, st)
+                 : launch_mode<MODE_DOWN, 1>(mA, mB, mB, g, rows, sms, st);
+}
 
 cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t between_gemms) {
   if (p.rows == 0) return cudaSuccess;

@@ -62,6 +62,8 @@ struct WsLayout {
   size_t ec_band;                        // [E,T] int32
   size_t ec_h64;                         // [E,T] fp64
   size_t ec_sel;                         // [E*Cp] int32
+  size_t rt_scratch;                     // tensor-core router filter (bf16 token choice)
+  size_t rt_scratch_bytes;
   int32_t ec_cp;                         // min(C, T)
   size_t idx, w, pos;        // [T,k] int32 / fp32 / int32
   size_t row_of;             // [T,k] int32: expert-grouped row of each assignment, -1 if dropped
@@ -111,8 +113,14 @@ struct RouterParams {
   int gate_raw;     // 1: gates are the full-softmax probabilities of the selected experts
   long long* stats;
   int* err;
+  void* scratch;    // workspace room for the tensor-core filter path (null: CUDA cores only)
+  size_t scratch_bytes;
 };
 cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st);
+// the tensor-core filter router (router_tc.cu) for wide logit tables of bf16 layers
+bool router_tc_applies(const RouterParams& p, int dtype);
+size_t router_tc_scratch_bytes(long long T, int d, int E);
+cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t st);
 // the cluster-tiled router kernel (router_tiled.cu), for wide logit tables
 cudaError_t launch_router_tiled(const RouterParams& p, int dtype, cudaStream_t st, int sms);
 
@@ -182,6 +190,9 @@ struct FfnParams {
 // between_gemms (optional) is recorded on `st` after the first GEMM is enqueued
 cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t between_gemms = nullptr);
 cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st);
+// out[r, n] = sum_k A[r, k mod Ka] * B[n, k] on the tensor cores (bf16 in, fp32 out)
+cudaError_t launch_dense_wrapped_gemm(const void* A, long long rows, int Ka, const void* B, int N, int K, float* out,
+                                      int* err, cudaStream_t st);
 
 struct CombineParams {
   const float* y_perm;

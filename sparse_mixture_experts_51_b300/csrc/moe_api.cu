@@ -54,6 +54,8 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.ec_band = take(sizeof(int32_t) * TE);
   L.ec_h64 = take(sizeof(double) * TE);
   L.ec_sel = take(ec ? sizeof(int32_t) * static_cast<size_t>(L.rows) : 0);
+  L.rt_scratch_bytes = (s.dtype == MOE_BF16 && !ec) ? router_tc_scratch_bytes(s.T, s.d, s.E) : 0;
+  L.rt_scratch = take(L.rt_scratch_bytes);
   L.idx = take(sizeof(int32_t) * Tk);
   L.w = take(sizeof(float) * Tk);
   L.pos = take(sizeof(int32_t) * Tk);
@@ -170,7 +172,8 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g
 // expert of each token when overflow re-routing is on.
 static moe_status_t route_impl(const moe_shape_t* shape, const void* x, const float* W_g, const float* b_g,
                                const float* W_noise, const float* eps, int32_t* idx, float* w, float* logits,
-                               int64_t* stats, int32_t* backup, int* err, cudaStream_t st) {
+                               int64_t* stats, int32_t* backup, int* err, cudaStream_t st, void* scratch = nullptr,
+                               size_t scratch_bytes = 0) {
   if (shape->T == 0) return MOE_OK;
   RouterParams p{};
   p.x = x;
@@ -189,6 +192,8 @@ static moe_status_t route_impl(const moe_shape_t* shape, const void* x, const fl
   p.gate_raw = shape->gates == MOE_GATES_RAW ? 1 : 0;
   p.stats = reinterpret_cast<long long*>(stats);
   p.err = err;
+  p.scratch = scratch;
+  p.scratch_bytes = scratch_bytes;
   return cuda_status(launch_router(p, shape->dtype, st));
 }
 
@@ -600,7 +605,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     cshape.k = shape->E;
   } else {
     int32_t* backup = shape->overflow == MOE_OVERFLOW_REROUTE ? at<int32_t>(ws, L.rr_backup) : nullptr;
-    if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s)) != MOE_OK)
+    if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s,
+                         at<void>(ws, L.rt_scratch), L.rt_scratch_bytes)) != MOE_OK)
       return st;
     if ((st = mark(1)) != MOE_OK) return st;
     if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,

@@ -214,7 +214,8 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
       g[0] = lane < E ? myred[u * NC + lane] : 0.f;
       z[0] = (p.W_n != nullptr && lane < E) ? myred[u * NC + E + lane] : 0.f;
       auto wcol = [&](int c, int j) { return *reinterpret_cast<const float4*>(&Wt[c * ldw + j]); };
-      rank_token<TX, 1>(p, t, lane, g, z, ep[u], sqrtf(myred[32 + u]), cn2, gam, wcol, n_recomputed, n_near);
+      const float xb[1] = {0.f};
+      rank_token<TX, 1>(p, t, lane, g, z, ep[u], sqrtf(myred[32 + u]), cn2, gam, wcol, n_recomputed, n_near, xb);
     }
     __syncwarp();
   }
@@ -294,6 +295,10 @@ cudaError_t launch_typed(const RouterParams& p, int dtype, cudaStream_t st, cons
 }  // namespace
 
 cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st) {
+  // wide logit tables of long bf16 batches: the tensor-core filter path
+  if (p.T > 0 && p.scratch != nullptr && router_tc_applies(p, dtype) &&
+      p.scratch_bytes >= router_tc_scratch_bytes(p.T, p.d, p.E))
+    return launch_router_tc(p, p.scratch, st);
   if (p.T == 0) return cudaSuccess;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

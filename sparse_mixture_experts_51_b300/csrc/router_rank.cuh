@@ -145,11 +145,13 @@ __device__ __forceinline__ void load_eps(const RouterParams& p, long long t, int
 // logits when asked); n_recomputed / n_near count settled-in-fp64 tokens and
 // near ties (warp-uniform).
 // ep[s] is eps[t, lane + 32 s] (loaded early by the caller; unused without noise).
+// xb[s] is added to that expert's error bound (a caller whose value for the
+// expert came from elsewhere states its error there; 0 otherwise).
 template <typename TX, int SLOTS, typename WCol>
 __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, int lane, const float (&g)[SLOTS],
                                            const float (&z)[SLOTS], const float (&ep_in)[SLOTS], float nx,
                                            const float* cn, float gam, WCol wcol, int& n_recomputed,
-                                           int& n_near) {
+                                           int& n_near, const float (&xb)[SLOTS]) {
   const int E = p.E, k = p.k, d = p.d;
   // ranks settled exactly: the top k, and the (k+1)-th too when the backup is asked for
   const int kr = (p.backup != nullptr && k < E) ? k + 1 : k;
@@ -179,7 +181,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
       if (p.logits) p.logits[t * E + e] = h;
       if (h != h) h = -INFINITY;  // NaN ranks last
       H[s] = h;
-      B[s] = bound * 1.25f + 1e-30f;
+      B[s] = (bound + xb[s]) * 1.25f + 1e-30f;
       if (p.radius) p.radius[t * E + e] = B[s];
     }
   }

@@ -316,7 +316,10 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
         }
       }
     }
-    rank_token<TX, SLOTS>(p, t, lane, g, z, ep_cur, sqrtf(nx2), cn2f, gam, wcol, n_recomputed, n_near);
+    float xb[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) xb[s] = 0.f;
+    rank_token<TX, SLOTS>(p, t, lane, g, z, ep_cur, sqrtf(nx2), cn2f, gam, wcol, n_recomputed, n_near, xb);
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) ep_cur[s] = ep_next[s];
   }
