@@ -85,11 +85,26 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
   auto wcol = [&](int c, int j) { return __ldg(reinterpret_cast<const float4*>(wt + static_cast<long long>(c) * d + j)); };
 
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-  for (long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < p.T;
-       t += nwarps) {
-    const __nv_bfloat16* xrow = x + t * d;
-    float ep[SLOTS];
+  // the approximate logits and the noise of a token, requested one token ahead
+  auto load_tok = [&](long long t, float (&ga)[SLOTS], float (&za)[SLOTS], float (&ep)[SLOTS]) {
     load_eps<SLOTS>(p, t, lane, ep);
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) {
+      const int e = lane + 32 * s;
+      const bool ok = t < p.T && e < E;
+      ga[s] = ok ? __ldg(approx + t * nc + e) : 0.f;
+      za[s] = (ok && noisy) ? __ldg(approx + t * nc + E + e) : 0.f;
+    }
+  };
+  long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  float ga_n[SLOTS], za_n[SLOTS], ep_n[SLOTS];
+  load_tok(t, ga_n, za_n, ep_n);
+  for (; t < p.T; t += nwarps) {
+    const __nv_bfloat16* xrow = x + t * d;
+    float ga[SLOTS], za[SLOTS], ep[SLOTS];
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) { ga[s] = ga_n[s]; za[s] = za_n[s]; ep[s] = ep_n[s]; }
+    load_tok(t + nwarps, ga_n, za_n, ep_n);
     // ---- token norm
     float sq = 0.f;
     for (int j = lane * 4; j < d; j += 128) {
@@ -106,11 +121,11 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
       g[s] = z[s] = xb[s] = 0.f;
       lo[s] = up[s] = -INFINITY;
       if (e < E) {
-        g[s] = __ldg(approx + t * nc + e);
+        g[s] = ga[s];
         float h = g[s] + (p.b_g ? __ldg(p.b_g + e) : 0.f);
         float dl = kFilterMargin * nx * s_cn[e];
         if (noisy) {
-          z[s] = __ldg(approx + t * nc + E + e);
+          z[s] = za[s];
           h += ep[s] * softplus_f32(z[s]);
           dl += fabsf(ep[s]) * kFilterMargin * nx * s_cn[E + e];  // softplus is 1-Lipschitz
         }
