@@ -12,7 +12,8 @@
 // v + r < L is not; the remaining band is re-evaluated in fp64 and the
 // missing places are filled from it by (fp64 score, token index).
 //
-// One 1024-thread block per expert: two 4-pass radix selects (8-bit digits,
+// One 1024-thread block per expert (the column's bound keys cached in shared
+// memory up to 24576 tokens): two 4-pass radix selects (8-bit digits,
 // both bounds at once) over the expert's column, an ordered compaction of
 // the band, fp64 dot products (a warp per band token), the band ranking,
 // and an ordered pass that numbers the chosen tokens in token order: row
@@ -28,6 +29,7 @@ using router_detail::softplus_f64;
 
 constexpr int ET = 1024;  // threads per block
 constexpr int EW = ET / 32;
+constexpr int kEcCacheTokens = 24576;  // up to this T the column's bound keys stay in shared memory (192 KB)
 
 // order-preserving maps (a larger value has a larger key; NaN ranks as -inf)
 __device__ __forceinline__ uint32_t fkey(float f) {
@@ -110,19 +112,33 @@ __global__ void __launch_bounds__(ET, 1) ec_select_kernel(EcParams p) {
   __shared__ int s_dig[2], s_rem[2];
   __shared__ double s_h[ET];
   __shared__ int s_t[ET];
+  extern __shared__ uint32_t s_keys[];  // [2][T] when T <= kEcCacheTokens: lower, upper keys
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
   const int T = p.T, E = p.E, Cp = p.Cp;
+  const bool cached = T <= kEcCacheTokens;
   uint8_t* flag = p.flag + static_cast<long long>(e) * T;
   int32_t* band = p.band + static_cast<long long>(e) * T;
   double* h64 = p.h64 + static_cast<long long>(e) * T;
   pdl_wait();  // logits, radii and lse come from the router
 
-  auto lo_hi = [&](int t, uint32_t& klo, uint32_t& khi) {
+  auto lo_hi_global = [&](int t, uint32_t& klo, uint32_t& khi) {
     const float v = __ldg(p.logits + static_cast<long long>(t) * E + e);
     const float r = __ldg(p.radius + static_cast<long long>(t) * E + e);
     klo = fkey(__fsub_rd(v, r));
     khi = fkey(__fadd_ru(v, r));
+  };
+  if (cached) {
+    for (int t = tid; t < T; t += ET) lo_hi_global(t, s_keys[t], s_keys[T + t]);
+    __syncthreads();
+  }
+  auto lo_hi = [&](int t, uint32_t& klo, uint32_t& khi) {
+    if (cached) {
+      klo = s_keys[t];
+      khi = s_keys[T + t];
+    } else {
+      lo_hi_global(t, klo, khi);
+    }
   };
 
   if (Cp == 0 || Cp >= T) {
@@ -339,11 +355,18 @@ __global__ void __launch_bounds__(256) ec_gather_kernel(EcParams p, const void* 
 
 }  // namespace
 
+template <typename TX>
+cudaError_t launch_ec_select_t(const EcParams& p, cudaStream_t st) {
+  const size_t smem = p.T <= kEcCacheTokens ? sizeof(uint32_t) * 2 * static_cast<size_t>(p.T) : 0;
+  cudaError_t e = cudaFuncSetAttribute(ec_select_kernel<TX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(uint32_t) * 2 * kEcCacheTokens));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(ec_select_kernel<TX>, dim3(static_cast<unsigned>(p.E)), dim3(ET), smem, st, 1, p);
+}
+
 cudaError_t launch_ec_select(const EcParams& p, int dtype, cudaStream_t st) {
   if (p.E == 0 || p.T == 0) return cudaSuccess;
-  if (dtype == MOE_BF16)
-    return launch_pdl(ec_select_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(p.E)), dim3(ET), 0, st, 1, p);
-  return launch_pdl(ec_select_kernel<float>, dim3(static_cast<unsigned>(p.E)), dim3(ET), 0, st, 1, p);
+  return dtype == MOE_BF16 ? launch_ec_select_t<__nv_bfloat16>(p, st) : launch_ec_select_t<float>(p, st);
 }
 
 cudaError_t launch_ec_finalize(const EcParams& p, int32_t* counts, int32_t* offsets, long long* dropped,
