@@ -462,41 +462,69 @@ def run_ours(a):
                 "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy bandwidth",
                 "algorithmic_bytes": nbytes, "ms_per_launch": g1_ms, "traffic": traffic}
 
-    # ---------------- end to end through the public API with host buffers
+    # ---------------- end to end through the public API with host buffers.
+    # Every step copies its tokens (and noise) from pinned host memory, runs
+    # the layer (MoELayer, the public call) and reads the output back to
+    # pinned host memory.  Like a serving loop the steps are pipelined on
+    # three streams with two device buffer sets: the input copy of step i+1
+    # and the output copy of step i-1 overlap the layer of step i.  The timed
+    # region spans the first input copy to the last output copy; no L2 flush
+    # (every step's inputs arrive from the host, and the expert weights are
+    # read from HBM each step).
     layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
                          b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False,
                          routing=w.routing, **(shared_t if Fsh else {}))
     x_host = inp["x"].pin_memory()
     eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
-    out_host = torch.empty(w.T, w.d, dtype=w.dtype).pin_memory()
-    x_dev = torch.empty_like(g["x"])
-    eps_dev = torch.empty_like(g["eps"]) if g["eps"] is not None else None
-    out_dev = torch.empty_like(out)
+    out_host = [torch.empty(w.T, w.d, dtype=w.dtype).pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(g["x"]) for _ in range(2)]
+    eps_dev = [torch.empty_like(g["eps"]) if g["eps"] is not None else None for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        if eps_dev is not None:
-            eps_dev.copy_(eps_host, non_blocking=True)
-        layer(x_dev, eps=eps_dev, out=out_dev)
-        out_host.copy_(out_dev, non_blocking=True)
+    def e2e_run(n):
+        """n pipelined steps; returns the elapsed ms from the first input copy to the last output copy."""
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+        in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        s_in.wait_event(t0)
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[b])  # the layer of step i-2 has read this buffer
+                x_dev[b].copy_(x_host, non_blocking=True)
+                if eps_host is not None:
+                    eps_dev[b].copy_(eps_host, non_blocking=True)
+                in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_done[b])  # the output of step i-2 has left this buffer
+            layer(x_dev[b], eps=eps_dev[b], out=out_dev[b], stream=stream)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                out_host[b].copy_(out_dev[b], non_blocking=True)
+                out_done[b].record(s_out)
+        stream.wait_event(out_done[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(out_done[n % 2])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
 
-    for _ in range(max(1, a.warmup)):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = 0.0
-    n_e2e = max(1, a.steps)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
-    for i in range(n_e2e):
-        flush.zero_()
-        evs[i][0].record(stream)
-        e2e_step()
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in evs), world, dev)
+    e2e_run(max(2, a.warmup))
+    n_e2e = max(2, a.steps)
+    e2e_ms = max_over_ranks(e2e_run(n_e2e), world, dev)
+    # the layer run through the public call gives the device-timed output, bit for bit
+    if not torch.equal(out_host[(n_e2e - 1) % 2], out.cpu()):
+        raise RuntimeError("end-to-end output differs from the timed layer's output")
     h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
     e2e = {"value": job_throughput(w.T, n_e2e, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h}
+           "d2h_bytes_per_step": d2h, "pipelined": "input copy of step i+1 and output copy of step i-1 overlap "
+                                                   "the layer of step i (two buffer sets, three streams)"}
 
     # ---------------- routing diagnostics + aux loss of the same batch (moe_routing_stats,
     # a separate call after the layer; token-choice routing only, it needs a top-k table)
