@@ -303,6 +303,14 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const floa
  *   shared  moe_shared_t* | NULL: the shared experts' weights, required iff
  *           shape->d_ff_shared > 0; their FFN runs first (on every token)
  *           and its output is added in the combine
+ * Routing is as in moe_route.  For long bf16 batches (T >= 16384) whose
+ * logit table has 32..256 columns (E, or 2E with noise), when no logits
+ * output is asked for and the gates are renormalised, the router first
+ * filters the experts with a tensor-core pass (weights split into two bf16
+ * parts, fp32 accumulation) and a margin of 2^-10 ||x|| ||w_col||, then
+ * ranks the remaining candidates exactly as moe_route does; the margin
+ * assumes the tensor core's fp32 accumulation of exact bf16 products loses
+ * fewer than about ten of fp32's 24 bits per step.
  * With overflow re-routing (shape->overflow) idx holds, for each
  * assignment, the expert it was finally sent to (the backup for a re-routed
  * one), pos its slot there, dropped the assignments left without an expert.
