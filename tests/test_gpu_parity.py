@@ -187,3 +187,50 @@ def test_cuda_graph_replay_matches_eager():
     out2 = cap.replay().clone()
     torch.cuda.synchronize()
     assert torch.equal(out2, layer(x2))
+
+
+def test_forward_timed_stage_events():
+    """moe_forward_timed writes what moe_forward writes, and its six stage
+    events (some NULL) record in order, eagerly and inside a CUDA graph."""
+    import ctypes
+
+    from sparse_mixture_experts_51_b300 import _lib
+
+    w = W.WORKLOADS["bf16_t4096"].scaled(1024)
+    inp = W.make_inputs(w)
+    g = to_gpu(inp)
+    C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
+    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, "swiglu")
+    ws = api.new_workspace(shape, C, "cuda")
+    lib = _lib.load()
+    P = api._ptr
+
+    def run(fn, out, *extra):
+        s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        args = [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), None, None, None,
+                P(g["W1"]), P(g["W3"]), P(g["W2"]), None, None, None, P(out)] + [None] * 9 + [P(ws), ws.numel(), s]
+        _lib.check(fn(*args, *extra), fn.__name__)
+
+    ref = torch.empty(w.T, w.d, dtype=w.dtype, device="cuda")
+    run(lib.moe_forward, ref)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record()
+    torch.cuda.synchronize()
+    arr = (ctypes.c_void_p * 6)(*[e.cuda_event if i != 4 else None for i, e in enumerate(evs)])
+    out = torch.empty_like(ref)
+    run(lib.moe_forward_timed, out, arr)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    spans = [evs[i].elapsed_time(evs[j]) for i, j in [(0, 1), (1, 2), (2, 3), (3, 5)]]
+    assert all(sp >= 0 for sp in spans) and evs[0].elapsed_time(evs[5]) > 0
+    # the same call captured into a graph: its events become external nodes that time every replay
+    out2 = torch.zeros_like(ref)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(lib.moe_forward_timed, out2, arr)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out2, ref)
+    assert evs[0].elapsed_time(evs[5]) > 0
+    assert api.get_device_error(ws) == 0
