@@ -378,8 +378,9 @@ MOE_API moe_status_t moe_forward_timed(const moe_shape_t* shape, double capacity
  *                                 kept assignment
  *                             [5] overflow: dropped / (T*k)
  *   ws, ws_bytes  the workspace of moe_workspace_size(shape, C) for any C
- * T = 0 gives all zeros.  One kernel; the softmax is taken in fp32, every
- * sum in fp64 in a fixed order, so results are deterministic.  An expert id
+ * T = 0 gives all zeros.  One kernel; the softmax is taken in fp32 and the
+ * sums are exact fixed-point integer sums (each probability rounded to a
+ * multiple of 2^-(62 - bits(T))), so results are deterministic.  An expert id
  * outside [0,E) is counted nowhere and sets MOE_ERR_BOUNDS in the error
  * word.  Calls that share a workspace must be ordered on one stream. */
 MOE_API moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, const int32_t* idx,

@@ -50,8 +50,7 @@ struct WsLayout {
   size_t disp_agg;   // int32 [nblk][E] per-block expert histograms
   size_t disp_incl;  // int32 [nblk][E] inclusive prefixes
   size_t stats_ticket;  // int32 last-block ticket of moe_routing_stats (self-resetting)
-  size_t stats_part;    // fp64 [kStatsMaxBlocks][E+1] per-block sums of p (and entropy)
-  size_t stats_load;    // int32 [kStatsMaxBlocks][E] per-block routed loads
+  size_t stats_acc;     // uint64 [2E+1] fixed-point totals of p, entropy and routed loads
   size_t h_shared;      // [T,d_ff_shared] dtype: hidden activation of the shared experts
   size_t y_shared;      // [T,d] fp32: shared experts' output
   // expert-choice routing only (zero size otherwise)
@@ -248,8 +247,7 @@ struct StatsParams {
   double* f;        // [E] out
   double* P;        // [E] out
   double* summary;  // [6] out
-  double* part;     // [kStatsMaxBlocks][E+1]
-  int* load_part;   // [kStatsMaxBlocks][E]
+  unsigned long long* acc;  // [2E+1] fixed-point totals (zero between calls)
   int* ticket;
   int* err;
 };

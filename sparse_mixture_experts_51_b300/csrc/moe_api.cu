@@ -39,8 +39,7 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.disp_agg = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
   L.disp_incl = take(sizeof(int) * static_cast<size_t>(L.nblk_dispatch) * s.E);
   L.stats_ticket = take(sizeof(int));
-  L.stats_part = take(sizeof(double) * static_cast<size_t>(kStatsMaxBlocks) * (s.E + 1));
-  L.stats_load = take(sizeof(int) * static_cast<size_t>(kStatsMaxBlocks) * s.E);
+  L.stats_acc = take(sizeof(unsigned long long) * (2 * static_cast<size_t>(s.E) + 1));
   // (the regions up to here do not depend on C: any C's workspace holds them)
   L.h_shared = take(b * static_cast<size_t>(s.T) * s.d_ff_shared);
   L.y_shared = take(s.d_ff_shared > 0 ? sizeof(float) * static_cast<size_t>(s.T) * s.d : 0);
@@ -689,8 +688,7 @@ moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, co
   p.f = f;
   p.P = P;
   p.summary = summary;
-  p.part = at<double>(ws, L.stats_part);
-  p.load_part = at<int>(ws, L.stats_load);
+  p.acc = at<unsigned long long>(ws, L.stats_acc);
   p.ticket = at<int>(ws, L.stats_ticket);
   p.err = at<int>(ws, L.err);
   return cuda_status(launch_routing_stats(p, static_cast<cudaStream_t>(stream)));

@@ -11,12 +11,16 @@
 //
 // One kernel, deterministic: one wave of blocks, block b taking a
 // contiguous run of tokens; a warp per token (four in flight) forms the
-// softmax of its logits in fp32 (lane holds experts lane + 32 s) and adds p
-// and the token's entropy to fp64 sums in token order; the block histograms
-// its tokens' selected experts in shared memory (integer adds).  Warps,
-// then blocks, are summed in a fixed order; the last block to finish (a
-// ticket) reduces the per-block partials with every thread, writes f, P
-// and the summary, and clears the ticket for the next call.
+// softmax of its logits in fp32 (lane holds experts lane + 32 s).  Every sum
+// is an exact integer sum, so its order does not matter: each probability is
+// added as the fixed-point integer round(p * 2^sp) (sp = 62 - bits(T), so the
+// sum of T of them fits in 63 bits; error at most 2^-(sp+1) per token), each
+// token's entropy as round(h * 2^sh) (h <= ln 128 < 8), each selected expert
+// as a count.  Lanes, then the block (shared-memory atomics), then the grid
+// (global atomics) add them up; the last block to finish (a ticket) turns
+// the totals into f, P and the summary in fp64, then clears the totals and
+// the ticket for the next call.  (B300's fp64 pipe is slow: long fp64 add
+// chains cost more than the whole rest of the kernel.)
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,7 +30,6 @@ namespace {
 constexpr int SB = 256;  // threads per block
 constexpr int SW = SB / 32;
 constexpr int TPW = 4;   // tokens a warp has in flight
-constexpr int SLOTS = kMaxExperts / 32;
 
 // Sum of v over the 32 lanes in a fixed butterfly order (deterministic).
 __device__ __forceinline__ double warp_sum_fixed(double v) {
@@ -35,12 +38,18 @@ __device__ __forceinline__ double warp_sum_fixed(double v) {
   return v;
 }
 
+__device__ __forceinline__ int bit_length(long long v) {
+  int b = 0;
+  while (v > 0) { ++b; v >>= 1; }
+  return b;
+}
+
+// SLOTS: 32-expert slots a lane holds (E <= 32 * SLOTS)
+template <int SLOTS>
 __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
-  __shared__ double s_p[SW][kMaxExperts + 1];  // per-warp sums of p (column E: entropy)
+  __shared__ unsigned long long s_p[kMaxExperts], s_h;
   __shared__ int s_load[kMaxExperts];
-  __shared__ double s_red[2][SB];              // last block: per-thread partial sums
   __shared__ double s_P[kMaxExperts], s_ld[kMaxExperts], s_cnt[kMaxExperts];
-  __shared__ double s_ent_total;
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = p.E, k = p.k;
@@ -48,22 +57,31 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
   const int nb = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
   const long long per = (T + nb - 1) / nb;
   const long long t0 = b * per, t1 = min(T, t0 + per);
+  // fixed-point scales: T * 2^sp < 2^62 and T * 8 * 2^sh < 2^62
+  const int tb = bit_length(T);
+  const int sp = 62 - tb, sh = 59 - tb;
+  unsigned long long* acc_p = p.acc;            // [E]
+  unsigned long long* acc_h = p.acc + E;        // [1]
+  unsigned long long* acc_ld = p.acc + E + 1;   // [E]
 
-  for (int e = tid; e < kMaxExperts; e += SB) s_load[e] = 0;
+  for (int e = tid; e < kMaxExperts; e += SB) {
+    s_p[e] = 0ull;
+    s_load[e] = 0;
+  }
+  if (tid == 0) s_h = 0ull;
   pdl_wait();  // logits, top-k table and dispatch counts come from the predecessors
   __syncthreads();
 
   // ---- probability mass and entropy: warp w takes tokens t0 + w + SW*j,
   // TPW of them per round with every load issued before any arithmetic
-  double acc[SLOTS];
+  unsigned long long up[SLOTS], uh = 0ull;
 #pragma unroll
-  for (int s = 0; s < SLOTS; ++s) acc[s] = 0.0;
-  double ent = 0.0;
-  for (long long tb = t0 + warp; tb < t1; tb += static_cast<long long>(SW) * TPW) {
+  for (int s = 0; s < SLOTS; ++s) up[s] = 0ull;
+  for (long long tb0 = t0 + warp; tb0 < t1; tb0 += static_cast<long long>(SW) * TPW) {
     float l[TPW][SLOTS];
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
-      const long long t = tb + static_cast<long long>(u) * SW;
+      const long long t = tb0 + static_cast<long long>(u) * SW;
 #pragma unroll
       for (int s = 0; s < SLOTS; ++s) {
         const int e = lane + 32 * s;
@@ -72,7 +90,7 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
     }
 #pragma unroll
     for (int u = 0; u < TPW; ++u) {
-      if (tb + static_cast<long long>(u) * SW >= t1) break;  // warp-uniform
+      if (tb0 + static_cast<long long>(u) * SW >= t1) break;  // warp-uniform
       float m = l[u][0];
 #pragma unroll
       for (int s = 1; s < SLOTS; ++s) m = fmaxf(m, l[u][s]);
@@ -90,16 +108,17 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
 #pragma unroll
       for (int s = 0; s < SLOTS; ++s) {
         const float pr = ex[s] * inv;
-        acc[s] += static_cast<double>(pr);
+        up[s] += __float2ull_rn(ldexpf(pr, sp));
         if (pr > 0.f) h -= pr * logf(pr);
       }
-      ent += static_cast<double>(warp_sum(h));
+      h = warp_sum(h);
+      if (lane == 0) uh += __float2ull_rn(ldexpf(fmaxf(h, 0.f), sh));
     }
   }
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s)
-    if (lane + 32 * s < E) s_p[warp][lane + 32 * s] = acc[s];
-  if (lane == 0) s_p[warp][E] = ent;
+    if (lane + 32 * s < E && up[s] != 0ull) atomicAdd(&s_p[lane + 32 * s], up[s]);
+  if (lane == 0 && uh != 0ull) atomicAdd(&s_h, uh);
 
   // ---- routed loads of this block's tokens (before the capacity cut)
   for (long long a = t0 * k + tid; a < t1 * k; a += SB) {
@@ -109,16 +128,12 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
   }
   __syncthreads();
 
-  // ---- this block's partials, warps summed in order
-  double* part = p.part + static_cast<long long>(b) * (E + 1);
-  int* lpart = p.load_part + static_cast<long long>(b) * E;
-  for (int e = tid; e <= E; e += SB) {
-    double v = 0.0;
-#pragma unroll
-    for (int w = 0; w < SW; ++w) v += s_p[w][e];
-    part[e] = v;
-    if (e < E) lpart[e] = s_load[e];
+  // ---- this block's totals into the grid's
+  for (int e = tid; e < E; e += SB) {
+    if (s_p[e] != 0ull) atomicAdd(acc_p + e, s_p[e]);
+    if (s_load[e] != 0) atomicAdd(acc_ld + e, static_cast<unsigned long long>(s_load[e]));
   }
+  if (tid == 0 && s_h != 0ull) atomicAdd(acc_h, s_h);
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(p.ticket, 1) == nb - 1;
@@ -126,51 +141,16 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
   if (!s_last) return;
   __threadfence();
 
-  // ---- last block.  Columns c = 0..E (E: entropy); G threads per column,
-  // thread j of column c sums blocks j, j+G, ... in order, then the G
-  // partial sums are added in order: a fixed order for a given (T, E).
-  const int ncol = E + 1;
-  const int G = SB / ncol;  // >= 1 since E <= 128 < SB
-  {
-    const int c = tid / G, j = tid - c * G;
-    double ps = 0.0, ls = 0.0;
-    if (c < ncol) {
-      for (int b0 = j; b0 < nb; b0 += 8 * G) {
-        double pv[8];
-        int lv[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int b2 = b0 + u * G;
-          pv[u] = b2 < nb ? __ldcg(p.part + static_cast<long long>(b2) * ncol + c) : 0.0;
-          lv[u] = (b2 < nb && c < E) ? __ldcg(p.load_part + static_cast<long long>(b2) * E + c) : 0;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          ps += pv[u];
-          ls += static_cast<double>(lv[u]);
-        }
-      }
-    }
-    s_red[0][tid] = ps;
-    s_red[1][tid] = ls;
-  }
-  for (int e = tid; e < E; e += SB) s_cnt[e] = static_cast<double>(__ldg(p.counts + e));
-  __syncthreads();
+  // ---- last block: f, P and the summary
   const double Td = static_cast<double>(T), TK = static_cast<double>(T) * k;
-  if (tid <= E) {
-    double ps = 0.0, ls = 0.0;
-    for (int j = 0; j < G; ++j) {
-      ps += s_red[0][tid * G + j];
-      ls += s_red[1][tid * G + j];
-    }
-    if (tid < E) {
-      s_P[tid] = T > 0 ? ps / Td : 0.0;
-      s_ld[tid] = ls;
-      p.P[tid] = s_P[tid];
-      p.f[tid] = T > 0 ? ls / TK : 0.0;
-    } else {
-      s_ent_total = ps;
-    }
+  const double inv_p = T > 0 ? 1.0 / (ldexp(1.0, sp) * Td) : 0.0;
+  for (int e = tid; e < E; e += SB) {
+    const unsigned long long ap = __ldcg(acc_p + e), al = __ldcg(acc_ld + e);
+    s_P[e] = static_cast<double>(ap) * inv_p;
+    s_ld[e] = static_cast<double>(al);
+    s_cnt[e] = static_cast<double>(__ldg(p.counts + e));
+    p.P[e] = s_P[e];
+    p.f[e] = T > 0 ? s_ld[e] / TK : 0.0;
   }
   __syncthreads();
   if (warp == 0) {
@@ -204,15 +184,19 @@ __global__ void __launch_bounds__(SB) routing_stats_kernel(StatsParams p) {
     lvar = warp_sum_fixed(lvar);
     kvar = warp_sum_fixed(kvar);
     if (lane == 0) {
+      const unsigned long long ah = __ldcg(acc_h);
       p.summary[0] = static_cast<double>(E) * aux;
-      p.summary[1] = T > 0 ? s_ent_total / Td : 0.0;
+      p.summary[1] = T > 0 ? static_cast<double>(ah) / (ldexp(1.0, sh) * Td) : 0.0;
       p.summary[2] = lmean > 0 ? sqrt(lvar / E) / lmean : 0.0;
       p.summary[3] = kmean > 0 ? sqrt(kvar / E) / kmean : 0.0;
       p.summary[4] = used / E;
       p.summary[5] = T > 0 ? static_cast<double>(*p.dropped) / TK : 0.0;
-      *p.ticket = 0;  // the next call starts from zero
     }
   }
+  __syncthreads();
+  // the next call starts from zero
+  for (int i = tid; i < 2 * E + 1; i += SB) p.acc[i] = 0ull;
+  if (tid == 0) *p.ticket = 0;
   pdl_trigger();
 }
 
@@ -226,7 +210,10 @@ int stats_blocks(long long T) {
 }
 
 cudaError_t launch_routing_stats(const StatsParams& p, cudaStream_t st) {
-  return launch_pdl(routing_stats_kernel, dim3(static_cast<unsigned>(stats_blocks(p.T))), dim3(SB), 0, st, 1, p);
+  const dim3 grid(static_cast<unsigned>(stats_blocks(p.T)));
+  if (p.E <= 32) return launch_pdl(routing_stats_kernel<1>, grid, dim3(SB), 0, st, 1, p);
+  if (p.E <= 64) return launch_pdl(routing_stats_kernel<2>, grid, dim3(SB), 0, st, 1, p);
+  return launch_pdl(routing_stats_kernel<4>, grid, dim3(SB), 0, st, 1, p);
 }
 
 }  // namespace moe
