@@ -99,7 +99,17 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
   long long t = static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   float ga_n[SLOTS], za_n[SLOTS], ep_n[SLOTS];
   load_tok(t, ga_n, za_n, ep_n);
+  // the token row two tokens ahead is pulled into L2 (its norm and the
+  // candidates' dot products read it; most of the load latency is DRAM)
+  auto prefetch_row = [&](long long tt) {
+    if (tt < p.T)
+      for (int j = lane * 64; j < d; j += 32 * 64)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(x + tt * d + j));
+  };
+  prefetch_row(t);
+  prefetch_row(t + nwarps);
   for (; t < p.T; t += nwarps) {
+    prefetch_row(t + 2 * nwarps);
     const __nv_bfloat16* xrow = x + t * d;
     float ga[SLOTS], za[SLOTS], ep[SLOTS];
 #pragma unroll
