@@ -95,6 +95,15 @@ struct TileInfo {
   int e, row0, rows_valid, n0;
 };
 
+// One 32-byte global store (a whole sector): each epilogue lane owns one row
+// of the tile, so 16-byte stores would fill only half of every sector they
+// touch.  The address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),
+               "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 template <int MODE, int MT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -277,6 +286,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int cfirst = MT == 2 ? 0 : (warp - 4) >> 2;   // first 32-column chunk
     constexpr int CSTEP = MT == 2 ? 1 : 2;
     const int rloc = msel * BM + q * 32 + lane;         // row inside the tile
+    // whole-sector stores when every row start is 32-byte aligned (column
+    // offsets are multiples of 32 elements)
+    constexpr int OUT_BYTES = MODE == MODE_DOWN ? 4 : 2;
+    const bool st32 =
+        ((reinterpret_cast<uintptr_t>(g.out) | static_cast<uintptr_t>(g.out_ld * OUT_BYTES)) & uintptr_t(31)) == 0;
     int acc = 0;
     uint32_t aphase = 0;
     int ecur = 0;
@@ -310,8 +324,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               h2[i] = __floats2bfloat162_rn(silu_f(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
                                             silu_f(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
             uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+            if (st32) {
+              st_global_32b(dst, pk[0], pk[1]);
+              st_global_32b(dst + 2, pk[2], pk[3]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+              for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+            }
           }
         }
       } else {
@@ -331,17 +350,30 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
             }
             uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+            if (st32) {
+              st_global_32b(dst, pk[0], pk[1]);
+              st_global_32b(dst + 2, pk[2], pk[3]);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+              for (int i = 0; i < 4; ++i) dst[i] = pk[i];
+            }
           } else {
             float* out = static_cast<float*>(g.out);
-            float4* dst = reinterpret_cast<float4*>(out + row * g.out_ld + col);
+            uint4 o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float4 o = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+              float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              if (bias) { o.x += bias[4 * i]; o.y += bias[4 * i + 1]; o.z += bias[4 * i + 2]; o.w += bias[4 * i + 3]; }
-              dst[i] = o;
+              if (bias) { f.x += bias[4 * i]; f.y += bias[4 * i + 1]; f.z += bias[4 * i + 2]; f.w += bias[4 * i + 3]; }
+              o[i] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
+            if (st32) {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_global_32b(dst + 2 * i, o[2 * i], o[2 * i + 1]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 8; ++i) dst[i] = o[i];
             }
           }
         };
