@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -55,8 +56,9 @@ struct Cfg {
   static constexpr int NACC = MT == 1 ? 2 : 1;  // accumulator buffers
   static constexpr int ACC_COLS = 256 * MT;     // TMEM columns per buffer
   static constexpr int TILE_M = BM * MT;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 1024 /*barriers etc*/ +
-                                    2 * (kMaxExperts + 1) * 4;
+  static constexpr int STAGING_BYTES = EPI_WARPS * 4096;  // epilogue output boxes, 4 KB per warp
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 /*align*/ + 256 /*barriers*/ +
+                                    (2 * kMaxExperts + 1) * 4 /*tile tables*/;
 };
 
 enum { MODE_GELU = 0, MODE_SWIGLU = 1, MODE_DOWN = 2 };
@@ -72,6 +74,7 @@ struct GemmArgs {
   int n_tiles;    // N tiles per expert
   void* out;      // bf16 h or fp32 y
   long long out_ld;
+  long long out_rows;  // allocated rows of out
   const float* bias;  // [E, N_out] or null
   int* err;
 };
@@ -107,7 +110,8 @@ __device__ __forceinline__ void st_global_32b(void* p, const uint4& a, const uin
 template <int MODE, int MT>
 __global__ void __launch_bounds__(NTHREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmB3, GemmArgs g) {
+                        const __grid_constant__ CUtensorMap tmB3, const __grid_constant__ CUtensorMap tmOut,
+                        GemmArgs g) {
   using C = Cfg<MT>;
   constexpr int STAGES = C::STAGES, A_BYTES = C::A_BYTES, STAGE_BYTES = C::STAGE_BYTES, NACC = C::NACC;
   constexpr int BN_OUT = MODE == MODE_SWIGLU ? 128 : 256;
@@ -115,7 +119,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   // 1024-byte align the tile ring (128-byte swizzle atoms)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* staging = smem + STAGES * STAGE_BYTES;  // [EPI_WARPS][4 KB], 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::STAGING_BYTES);
   uint64_t* full = bars;                 // [STAGES]
   uint64_t* empty = bars + STAGES;       // [STAGES]
   uint64_t* tfull = bars + 2 * STAGES;   // [2]
@@ -124,7 +129,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_total = reinterpret_cast<int*>(tmem_slot + 2);
-  int* s_tstart = reinterpret_cast<int*>(smem + STAGES * STAGE_BYTES + 256);  // [E+1]
+  int* s_tstart = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + 256);  // [E+1]
   int* s_mt = s_tstart + kMaxExperts + 1;                                        // [E]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -279,18 +284,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else if (warp >= 4) {
     // ================= epilogue =================
-    // MT = 1: warps w and w+4 share lane quarter w & 3, taking alternate
-    // 32-column chunks; MT = 2: warps 4-7 drain M tile 0, warps 8-11 M tile 1
+    // MT = 1: warps w and w+4 share lane quarter w & 3, each taking half of
+    // the 32-column chunks; MT = 2: warps 4-7 drain M tile 0, warps 8-11 M
+    // tile 1.  A warp whose 32 rows all lie in the segment stages its rows
+    // in shared memory as 32 x 128-byte boxes (two bf16 chunks or one fp32
+    // chunk) and writes each with one TMA store; a warp holding the segment's
+    // end writes its valid rows directly (TMA would also write the rows past
+    // the end, which belong to the next expert).
+    constexpr int NCH = BN_OUT / 32;               // 32-column chunks per tile
+    constexpr int WCH = MT == 2 ? NCH : NCH / 2;   // chunks per warp
+    constexpr int BOX_CH = MODE == MODE_DOWN ? 1 : 2;
     const int q = warp & 3;                             // TMEM lane quarter this warp may access
     const int msel = MT == 2 ? (warp - 4) >> 2 : 0;     // M tile of the CTA tile
-    const int cfirst = MT == 2 ? 0 : (warp - 4) >> 2;   // first 32-column chunk
-    constexpr int CSTEP = MT == 2 ? 1 : 2;
+    const int cfirst = MT == 2 ? 0 : ((warp - 4) >> 2) * WCH;
     const int rloc = msel * BM + q * 32 + lane;         // row inside the tile
-    // whole-sector stores when every row start is 32-byte aligned (column
-    // offsets are multiples of 32 elements)
+    // direct stores: whole 32-byte sectors when every row start is 32-byte
+    // aligned (column offsets are multiples of 32 elements)
     constexpr int OUT_BYTES = MODE == MODE_DOWN ? 4 : 2;
     const bool st32 =
         ((reinterpret_cast<uintptr_t>(g.out) | static_cast<uintptr_t>(g.out_ld * OUT_BYTES)) & uintptr_t(31)) == 0;
+    const uint32_t stg = smem_u32(staging + (warp - 4) * 4096);  // this warp's box, 1024-byte aligned
     int acc = 0;
     uint32_t aphase = 0;
     int ecur = 0;
@@ -305,42 +318,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const long long row = static_cast<long long>(ti.row0) + rloc;
       // a warp whose 32 rows all lie past the segment reads nothing
       const bool warp_rows = __any_sync(0xffffffffu, row_ok);
+      const bool warp_full = __all_sync(0xffffffffu, row_ok);
+      // the accumulator is released as soon as this warp's last TMEM load
+      // has completed: the math and stores of its last chunks overlap the
+      // next tile's MMAs
+      bool released = false;
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        released = true;
+      };
+      // writes this lane's row of 32-column chunk c (NV 16-byte units)
+      auto emit = [&](int c, const uint4* v, auto nv_tag) {
+        constexpr int NV = decltype(nv_tag)::value;
+        const int col = ti.n0 + c * 32;
+        if (col >= g.N_out) return;
+        if (warp_full) {
+          const int half = BOX_CH == 2 ? ((c - cfirst) & 1) : 0;  // place of the chunk in its box
+          if (half == 0) {
+            // the previous box's store has finished reading the buffer
+            if (lane == 0) bulk_wait_group_read<0>();
+            __syncwarp();
+          }
+          // 128-byte swizzle (16-byte unit u of row r at u ^ (r & 7), the
+          // layout the tensor map undoes): the 8 lanes of a store phase hit
+          // distinct banks
+          const uint32_t rowp = stg + static_cast<uint32_t>(lane * 128);
+#pragma unroll
+          for (int i = 0; i < NV; ++i)
+            st_shared_v4(rowp + static_cast<uint32_t>(((half * 4 + i) ^ (lane & 7)) << 4), v[i]);
+          if (half == BOX_CH - 1) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmOut, stg, col - half * 32, static_cast<int>(row - lane));
+              bulk_commit_group();
+            }
+          }
+        } else if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint8_t*>(g.out) +
+                                                (row * g.out_ld + col) * OUT_BYTES);
+          if (st32) {
+#pragma unroll
+            for (int i = 0; i < NV / 2; ++i) st_global_32b(dst + 2 * i, v[2 * i], v[2 * i + 1]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < NV; ++i) dst[i] = v[i];
+          }
+        }
+      };
+      using NV4 = std::integral_constant<int, 4>;
+      using NV8 = std::integral_constant<int, 8>;
       if (!warp_rows) {
       } else if constexpr (MODE == MODE_SWIGLU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
 #pragma unroll 1
-        for (int c = cfirst; c < BN_OUT / 32; c += CSTEP) {
+        for (int c = cfirst; c < cfirst + WCH; ++c) {
           // gate and up columns in flight together, one wait
           uint32_t gr[32], ur[32];
           tmem_ld32_issue(tbase + c * 32, gr);
           tmem_ld32_issue(tbase + 128 + c * 32, ur);
           tmem_wait_ld(gr, ur);
-          const int col = ti.n0 + c * 32;
-          if (row_ok && col < g.N_out) {
-            uint4 pk[4];
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+          if (c == cfirst + WCH - 1) release();
+          uint4 pk[4];
+          __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              h2[i] = __floats2bfloat162_rn(silu_f(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
-                                            silu_f(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
-            if (st32) {
-              st_global_32b(dst, pk[0], pk[1]);
-              st_global_32b(dst + 2, pk[2], pk[3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = pk[i];
-            }
-          }
+          for (int i = 0; i < 16; ++i)
+            h2[i] = __floats2bfloat162_rn(silu_f(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
+                                          silu_f(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
+          emit(c, pk, NV4{});
         }
       } else {
         // two 32-column chunks in flight per wait
         auto store_chunk = [&](int c, const uint32_t (&v)[32]) {
           const int col = ti.n0 + c * 32;
-          if (!(row_ok && col < g.N_out)) return;
-          const float* bias = g.bias ? g.bias + static_cast<long long>(ti.e) * g.N_out + col : nullptr;
+          const float* bias = (g.bias && col < g.N_out) ? g.bias + static_cast<long long>(ti.e) * g.N_out + col
+                                                        : nullptr;
           if constexpr (MODE == MODE_GELU) {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(g.out);
             uint4 pk[4];
             __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
@@ -349,16 +403,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (bias) { a0 += bias[2 * i]; a1 += bias[2 * i + 1]; }
               h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
             }
-            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
-            if (st32) {
-              st_global_32b(dst, pk[0], pk[1]);
-              st_global_32b(dst + 2, pk[2], pk[3]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) dst[i] = pk[i];
-            }
+            emit(c, pk, NV4{});
           } else {
-            float* out = static_cast<float*>(g.out);
             uint4 o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -367,31 +413,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (bias) { f.x += bias[4 * i]; f.y += bias[4 * i + 1]; f.z += bias[4 * i + 2]; f.w += bias[4 * i + 3]; }
               o[i] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
             }
-            uint4* dst = reinterpret_cast<uint4*>(out + row * g.out_ld + col);
-            if (st32) {
-#pragma unroll
-              for (int i = 0; i < 4; ++i) st_global_32b(dst + 2 * i, o[2 * i], o[2 * i + 1]);
-            } else {
-#pragma unroll
-              for (int i = 0; i < 8; ++i) dst[i] = o[i];
-            }
+            emit(c, o, NV8{});
           }
         };
 #pragma unroll 1
-        for (int c = cfirst; c < BN_OUT / 32; c += 2 * CSTEP) {
+        for (int c = cfirst; c < cfirst + WCH; c += 2) {
           uint32_t r0[32], r1[32];
           tmem_ld32_issue(tbase + c * 32, r0);
-          tmem_ld32_issue(tbase + (c + CSTEP) * 32, r1);
+          tmem_ld32_issue(tbase + (c + 1) * 32, r1);
           tmem_wait_ld(r0, r1);
+          if (c + 2 >= cfirst + WCH) release();
           store_chunk(c, r0);
-          store_chunk(c + CSTEP, r1);
+          store_chunk(c + 1, r1);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (!released) release();
       if (++acc == NACC) { acc = 0; aphase ^= 1u; }
     }
+    // every staged box has been written to global memory
+    if (lane == 0) bulk_wait_group_all();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -432,18 +473,35 @@ cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, int K, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Output tensor [rows, cols] (row stride ld elements, bf16 or fp32) written
+// by the epilogue in 128-byte x 32-row boxes, 128-byte swizzle.
+cudaError_t make_out_map(CUtensorMap* m, void* base, long long rows, int cols, long long ld, bool f32) {
+  const int esz = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esz), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int MODE, int MT>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b3, const GemmArgs& g,
                         long long rows_bound, int num_sms, cudaStream_t st) {
+  CUtensorMap o;
+  cudaError_t e = make_out_map(&o, g.out, g.out_rows, g.N_out, g.out_ld, MODE == MODE_DOWN);
+  if (e != cudaSuccess) return e;
   auto kern = grouped_gemm_kernel<MODE, MT>;
   constexpr int smem = Cfg<MT>::SMEM_BYTES;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // upper bound on tiles: every expert may add one partial M tile
   const long long mt_bound = (rows_bound + Cfg<MT>::TILE_M - 1) / Cfg<MT>::TILE_M + g.E;
   const long long tiles_bound = mt_bound * g.n_tiles;
   const int grid = static_cast<int>(std::min<long long>(num_sms, std::max<long long>(1, tiles_bound)));
-  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), static_cast<size_t>(smem), st, 1, a, b, b3, g);
+  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), static_cast<size_t>(smem), st, 1, a, b, b3, o, g);
 }
 
 }  // namespace
@@ -473,6 +531,7 @@ cudaError_t launch_dense_wrapped_gemm(const void* A, long long rows, int Ka, con
   g.n_tiles = (N + BN - 1) / BN;
   g.out = out;
   g.out_ld = N;
+  g.out_rows = rows;
   g.bias = nullptr;
   g.err = err;
   return MT == 2 ? launch_mode<MODE_DOWN, 2>(mA, mB, mB, g, rows, sms, st)
@@ -513,6 +572,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   g1.n_tiles = (p.F + (swiglu ? 127 : 255)) / (swiglu ? 128 : 256);
   g1.out = p.h;
   g1.out_ld = p.F;
+  g1.out_rows = p.rows;
   g1.bias = swiglu ? nullptr : p.b1;
   g1.err = p.err;
   if (MT == 2)
@@ -540,6 +600,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   g2.n_tiles = (p.d + 255) / 256;
   g2.out = p.y_perm;
   g2.out_ld = p.d;
+  g2.out_rows = p.rows;
   g2.bias = p.b2;
   g2.err = p.err;
   return MT == 2 ? launch_mode<MODE_DOWN, 2>(mA2, mB2, mB2, g2, p.rows, sms, st)
