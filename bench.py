@@ -38,7 +38,6 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer fwd tokens/s on 1 B300; TFLOP/s or HBM GB/s as % of roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "bf16_t4096"
-KERNELS_PER_STEP = 6  # router, dispatch, gather, expert GEMM 1, expert GEMM 2, combine
 FLUSH_BYTES = 256 << 20
 
 # DRAM traffic of the dominant kernel per launch, from an ncu capture
@@ -389,6 +388,12 @@ def run_ours(a):
         flush.zero_()
     torch.cuda.synchronize()
     assert api.get_device_error(ws) == 0
+    # kernels one step enqueues (the library counts its own launches; a graph
+    # replays exactly what one captured call enqueued)
+    n0 = lib.moe_kernel_launches()
+    _lib.check(lib.moe_forward(*fwd_args()), "moe_forward")
+    kernels_per_step = int(lib.moe_kernel_launches() - n0)
+    torch.cuda.synchronize()
 
     graphs = {}
 
@@ -626,7 +631,7 @@ def run_ours(a):
                                                      else "router_dispatch_gather"), "expert_gemm1",
                  "expert_gemm2_combine"], stage_ms)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (KERNELS_PER_STEP + (2 if Fsh else 0) + (1 if w.routing == "expert" else 0)) * a.steps,
+            "gpu_launches": kernels_per_step * a.steps,
             "clocks": sampler.summary(), "routing_stats": routing_stats}
     if shared_ffn is not None:
         line["shared_ffn"] = shared_ffn

@@ -392,6 +392,11 @@ MOE_API moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* lo
  * since the last read).  `ws` is the workspace passed to the calls. */
 MOE_API moe_status_t moe_get_device_error(void* ws, void* stream);
 
+/* Number of kernels the library has enqueued since it was loaded (every
+ * entry point, all threads).  Work that a CUDA graph replays is not
+ * enqueued again: count one captured call to know a graph's kernels. */
+MOE_API unsigned long long moe_kernel_launches(void);
+
 /* Static, human-readable name of a status code. */
 MOE_API const char* moe_status_string(moe_status_t status);
 

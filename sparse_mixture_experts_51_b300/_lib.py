@@ -62,6 +62,7 @@ SIGNATURES = {
                           + [ctypes.c_size_t, _P, ctypes.POINTER(ctypes.c_void_p)]),
     "moe_routing_stats": (ctypes.c_int, [_SHAPE] + [_P] * 8 + [ctypes.c_size_t, _P]),
     "moe_get_device_error": (ctypes.c_int, [_P, _P]),
+    "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_testing_dispatch_stalled": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 7
                                      + [ctypes.c_int32, _P, ctypes.c_size_t, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),

@@ -6,9 +6,21 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moe_b300.h"
 
 namespace moe {
+
+// Kernels this library has enqueued (moe_kernel_launches).
+inline std::atomic<unsigned long long>& launch_count() {
+  static std::atomic<unsigned long long> n{0};
+  return n;
+}
+inline cudaError_t counted(cudaError_t e) {
+  if (e == cudaSuccess) launch_count().fetch_add(1, std::memory_order_relaxed);
+  return e;
+}
 
 // Launch `kern` on `st` with programmatic stream serialisation (it may start
 // while the previous kernel on the stream finishes; the kernel calls
@@ -35,7 +47,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kern, args...);
+  return counted(cudaLaunchKernelEx(&cfg, kern, args...));
 }
 
 constexpr int kMaxExperts = 128;  // largest E the kernels support

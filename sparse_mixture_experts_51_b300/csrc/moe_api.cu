@@ -346,7 +346,7 @@ moe_status_t moe_route_expert_choice(const moe_shape_t* shape, int32_t C, const 
       return MOE_ERR_CUDA;
     ec_gates_kernel<<<static_cast<unsigned>((L.rows + 255) / 256), 256, 0, s>>>(ep.sel, ep.gate_te, shape->E,
                                                                                  L.ec_cp, gates);
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    if (counted(cudaGetLastError()) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (dropped != nullptr) {
     // counts / offsets are implied (C' each): the workspace copies take them
@@ -693,6 +693,8 @@ moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, co
   p.err = at<int>(ws, L.err);
   return cuda_status(launch_routing_stats(p, static_cast<cudaStream_t>(stream)));
 }
+
+unsigned long long moe_kernel_launches(void) { return launch_count().load(std::memory_order_relaxed); }
 
 moe_status_t moe_get_device_error(void* ws, void* stream) {
   if (ws == nullptr) return MOE_ERR_WORKSPACE;

@@ -364,7 +364,7 @@ cudaError_t launch_one_sl(const RouterParams& p, const TiledPlan& q, long long t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, p, q);
+  return counted(cudaLaunchKernelEx(&cfg, kern, p, q));
 }
 
 template <typename TX, int CQ, int TM>

@@ -234,3 +234,26 @@ def test_forward_timed_stage_events():
     assert torch.equal(out2, ref)
     assert evs[0].elapsed_time(evs[5]) > 0
     assert api.get_device_error(ws) == 0
+
+
+def test_kernel_launch_counter():
+    """moe_kernel_launches counts the kernels a call enqueues: six for a bf16
+    layer with the warp router (router, dispatch, gather, two expert GEMMs,
+    combine); replaying a captured call enqueues nothing new."""
+    from sparse_mixture_experts_51_b300 import _lib
+
+    lib = _lib.load()
+    w = W.WORKLOADS["bf16_t4096"].scaled(1024)
+    g = to_gpu(W.make_inputs(w))
+    layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, "swiglu", W3=g["W3"], capacity_factor=w.capacity_factor)
+    layer(g["x"])
+    torch.cuda.synchronize()
+    n0 = lib.moe_kernel_launches()
+    layer(g["x"])
+    assert lib.moe_kernel_launches() - n0 == 6
+    cap = layer.capture(g["x"])
+    n1 = lib.moe_kernel_launches()
+    for _ in range(3):
+        cap.replay()
+    torch.cuda.synchronize()
+    assert lib.moe_kernel_launches() == n1
