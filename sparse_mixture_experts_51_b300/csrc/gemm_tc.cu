@@ -16,9 +16,12 @@
 //               (per M tile), fp32 accumulator in TMEM; tcgen05.commit frees
 //               smem stages
 //   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
-//   warps 4-11  epilogue: two warps per TMEM lane quarter, each taking every
-//               other 32-column chunk: tcgen05.ld, fused activation, bias,
-//               conversion, row-masked 16-byte stores
+//   warps 4-11  epilogue: two warps per TMEM lane quarter (128-row tiles:
+//               half of the 32-column chunks each; 256-row tiles: one M tile
+//               each): tcgen05.ld, fused activation, bias, conversion; a
+//               warp whose rows all lie in the segment stages 128-byte boxes
+//               in shared memory and writes them with TMA stores, the warp
+//               at a segment's end stores its valid rows with 32-byte stores
 // SwiGLU puts 128 rows of W1 and the matching 128 rows of W3 into one
 // 256-row B tile, so one accumulator holds gate | up and the epilogue emits
 // 128 columns of h.  Tiles are ordered expert-major, then N, then M, so CTAs
