@@ -70,6 +70,14 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def step_quantiles(step_ms):
+    """Median and 95th percentile of the per-step device times (ms, this rank)."""
+    v = sorted(step_ms)
+    if not v:
+        return None
+    return {"p50": statistics.median(v), "p95": v[min(len(v) - 1, math.ceil(0.95 * len(v)) - 1)]}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -625,6 +633,7 @@ def run_ours(a):
                 "launch": "eager" if a.eager else f"CUDA graphs of up to {GRAPH_STEPS} timed steps (moe_forward_timed each)"})
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
             "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "step_ms_quantiles": step_quantiles(step_ms),
             "dtype": w.dtype_name, "data": "synthetic", "config": cfg,
             "stage_ms": {n: statistics.mean(v) for n, v in zip(
                 [("shared_ffn_" if Fsh else "") + ("router_select_gather" if w.routing == "expert"

@@ -58,3 +58,12 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     assert bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "0"])) == 0
     assert called == []
+
+
+def test_step_quantiles():
+    """Median and nearest-rank 95th percentile of per-step times."""
+    v = [float(i) for i in range(1, 21)]
+    q = bench.step_quantiles(list(reversed(v)))
+    assert q == {"p50": 10.5, "p95": 19.0}
+    assert bench.step_quantiles([0.25]) == {"p50": 0.25, "p95": 0.25}
+    assert bench.step_quantiles([]) is None
