@@ -48,6 +48,151 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, const fl
   *reinterpret_cast<uint2*>(p) = u;
 }
 
+// 32 bytes (a whole sector) from / to global memory in one access when `al`
+// (the address is 32-byte aligned), else as two 16-byte accesses.
+__device__ __forceinline__ void ld_g32(const void* p, uint4& a, uint4& b, bool al) {
+  if (al) {
+    asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+                 : "l"(p));
+  } else {
+    a = __ldg(static_cast<const uint4*>(p));
+    b = __ldg(static_cast<const uint4*>(p) + 1);
+  }
+}
+__device__ __forceinline__ void st_g32(void* p, const uint4& a, const uint4& b, bool al) {
+  if (al) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+                 "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+  } else {
+    static_cast<uint4*>(p)[0] = a;
+    static_cast<uint4*>(p)[1] = b;
+  }
+}
+__device__ __forceinline__ bool al32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+__device__ __forceinline__ void f8_from(const uint4& a, const uint4& b, float* f) {
+  f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+  f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y); f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+}
+__device__ __forceinline__ void f8_to(const float* f, uint4& a, uint4& b) {
+  a = make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  b = make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]), __float_as_uint(f[7]));
+}
+
+// 16-element chunks (d % 16 == 0): every operand moves in whole 32-byte
+// sectors.  One thread per (token, chunk); the chunk's offsets are multiples
+// of 32 bytes in every tensor, so a tensor's accesses are 32-byte aligned
+// exactly when its base address is.  Same arithmetic as combine_kernel.
+template <typename TO>
+__global__ void __launch_bounds__(256) combine16_kernel(CombineParams p, long long items, int chunks) {
+  pdl_wait();
+  pdl_trigger();
+  const long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (it >= items) return;
+  const long long t = it / chunks;
+  const int c = static_cast<int>(it - t * chunks) * 16;
+  const int k = p.k, d = p.d;
+  const TO* res = static_cast<const TO*>(p.residual);
+  float rv[16];
+  if (res) {
+    const bool al = al32(res);
+    if constexpr (sizeof(TO) == 2) {
+      uint4 a, b;
+      ld_g32(res + t * d + c, a, b, al);
+      auto widen = [&](uint32_t u, int i) {
+        rv[2 * i] = __uint_as_float(u << 16);
+        rv[2 * i + 1] = __uint_as_float(u & 0xffff0000u);
+      };
+      widen(a.x, 0); widen(a.y, 1); widen(a.z, 2); widen(a.w, 3);
+      widen(b.x, 4); widen(b.y, 5); widen(b.z, 6); widen(b.w, 7);
+    } else {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint4 a, b;
+        ld_g32(res + t * d + c + 8 * h, a, b, al);
+        f8_from(a, b, rv + 8 * h);
+      }
+    }
+  }
+  float sv[16];
+  if (p.y_shared) {
+    const bool al = al32(p.y_shared);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 a, b;
+      ld_g32(p.y_shared + t * d + c + 8 * h, a, b, al);
+      f8_from(a, b, sv + 8 * h);
+    }
+  }
+  const bool al_y = al32(p.y_perm);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 2
+  for (int r = 0; r < k; ++r) {
+    long long row = -1;
+    if (p.row_of) {
+      row = __ldg(p.row_of + t * k + r);
+    } else {
+      const int ps = __ldg(p.pos + t * k + r);
+      if (ps >= 0) {
+        const int e = __ldg(p.idx + t * k + r);
+        if (e >= 0 && e < p.E) row = static_cast<long long>(__ldg(p.offsets + e)) + ps;
+        if (row < 0) record_error(p.err, MOE_ERR_BOUNDS);
+      }
+    }
+    if (row < 0) continue;  // dropped: the residual carries the token
+    if (row >= p.rows) {
+      record_error(p.err, MOE_ERR_BOUNDS);
+      continue;
+    }
+    const float wt = __ldg(p.w + t * k + r);
+    float yv[16];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 a, b;
+      ld_g32(p.y_perm + row * d + c + 8 * h, a, b, al_y);
+      f8_from(a, b, yv + 8 * h);
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = fmaf(wt, yv[i], acc[i]);
+  }
+  if (p.y_shared) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] += sv[i];
+  }
+  if (p.moe_out) {
+    const bool al = al32(p.moe_out);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 a, b;
+      f8_to(acc + 8 * h, a, b);
+      st_g32(p.moe_out + t * d + c + 8 * h, a, b, al);
+    }
+  }
+  float o[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i] = res ? rv[i] + acc[i] : acc[i];
+  TO* out = static_cast<TO*>(p.out);
+  const bool al = al32(out);
+  if constexpr (sizeof(TO) == 2) {
+    auto pack = [&](int i) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      return *reinterpret_cast<const uint32_t*>(&h2);
+    };
+    st_g32(out + t * d + c, make_uint4(pack(0), pack(1), pack(2), pack(3)),
+           make_uint4(pack(4), pack(5), pack(6), pack(7)), al);
+  } else {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint4 a, b;
+      f8_to(o + 8 * h, a, b);
+      st_g32(out + t * d + c + 8 * h, a, b, al);
+    }
+  }
+}
+
 // One thread per (token, V-element chunk), V = 8 or 16: it resolves the
 // token's kept expert rows (from the grouped-row map when the dispatch wrote
 // one, else from idx / pos / offsets), issues every 16-byte load of the
@@ -251,10 +396,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st) {
     const long long items = static_cast<long long>(p.T) * chunks;
     const long long blocks = (items + 255) / 256;
     if (p.dtype == MOE_BF16)
-      return launch_pdl(combine_kernel<__nv_bfloat16, 16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p,
+      return launch_pdl(combine16_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p,
                         items, chunks);
     else
-      return launch_pdl(combine_kernel<float, 16>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, items,
+      return launch_pdl(combine16_kernel<float>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, 1, p, items,
                         chunks);
   } else if (p.d % 8 == 0) {
     const int chunks = p.d / 8;
