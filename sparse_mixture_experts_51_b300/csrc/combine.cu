@@ -5,9 +5,9 @@
 // output y_shared[t] when there is one  ("LLM part 09: Sparse
 // Mixture-of-Experts (MoE)", s1 output equation and s3 residual bypass of
 // dropped tokens; "Mixture-of-Experts Sparse Model Scaling", Lab 1 weighted
-// accumulation).  Each thread owns 8 consecutive elements of one token,
-// gathers them from its k expert rows with 16-byte loads and writes them
-// once: deterministic, no atomics, HBM-bound.
+// accumulation).  Each thread owns 16 (or 8) consecutive elements of one
+// token, gathers them from its k expert rows in whole 32-byte sectors (or
+// 16-byte loads) and writes them once: deterministic, no atomics, HBM-bound.
 //
 // fp32 FFN: the grouped expert MLP on CUDA cores for fp32 layers (whose
 // tolerance rules out tf32/bf16 tensor cores): one warp per output element,
@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(256) combine16_kernel(CombineParams p, long lo
   }
 }
 
-// One thread per (token, V-element chunk), V = 8 or 16: it resolves the
+// One thread per (token, V-element chunk) when d is a multiple of 8 but not
+// of 16 (V = 8; 16-element chunks use combine16_kernel): it resolves the
 // token's kept expert rows (from the grouped-row map when the dispatch wrote
 // one, else from idx / pos / offsets), issues every 16-byte load of the
 // chunk at once (k expert rows, the residual), and writes the chunk once.
