@@ -218,6 +218,7 @@ MOE_API moe_status_t moe_route_expert_choice(const moe_shape_t* shape, int32_t C
  *   x_perm    [moe_max_rows,d] dtype out   row offsets[e]+pos[t,r] = x[t]
  *   row_token [moe_max_rows] int32 | NULL  out: token of each row
  *   ws, ws_bytes  workspace (moe_workspace_size)
+ * x and x_perm must be 16-byte aligned (else MOE_ERR_UNSUPPORTED).
  * Results are deterministic (no atomics decide any slot).  An expert id
  * outside [0,E) sets MOE_ERR_BOUNDS in the error word; that assignment gets
  * pos = -1 and is counted in no load. */
@@ -242,9 +243,13 @@ MOE_API moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int
  * MOE_ERR_UNSUPPORTED before anything is enqueued.  The array (about
  * 257 KiB) stays resident on every GPU that loads the library until the
  * process exits.  It allocates nothing: no cudaMalloc, cudaFree or
- * allocating library call.  The first call on a device, with that device
- * current, looks up the array's device address (cudaGetSymbolAddress) and
- * caches it; make that first call before any stream capture.  All calls
+ * allocating library call.  It accepts exactly the shapes moe_dispatch
+ * accepts, and like moe_dispatch returns MOE_ERR_UNSUPPORTED for an x or
+ * x_perm that is not 16-byte aligned.  The first call in each CUDA context,
+ * with that context current, looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it under the context's process-unique
+ * id, so a context that is destroyed and recreated (cudaDeviceReset) gets a
+ * fresh lookup; make that first call before any stream capture.  All calls
  * share the one array and each call clears the parts that must start at
  * zero: calls whose kernels may overlap on the GPU (unordered streams,
  * several host threads) race on it and must be serialised by the caller. */

@@ -21,8 +21,13 @@
 // several host threads) race on it and must be serialised by the caller.
 //
 // Host code cannot use the array's name as a device address, so the first
-// call on each device (with that device current) looks the address up with
-// cudaGetSymbolAddress and caches it; later calls on that device reuse it.
+// call in each CUDA context (with that context current) looks the address up
+// with cudaGetSymbolAddress and caches it under the context's process-unique
+// id (cuCtxGetId); later calls in the same context reuse it.  A context that
+// is torn down and recreated (cudaDeviceReset, a new primary or non-primary
+// context) has a new id, so its first call looks the address up again.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -43,24 +48,61 @@ constexpr size_t kScratchInts = kInclOffset + static_cast<size_t>(kNoAllocMaxTil
 
 static __device__ __align__(256) int g_dispatch_scratch[kScratchInts];
 
-constexpr int kMaxCachedDevices = 64;
+constexpr int kMaxCachedContexts = 64;
+struct CachedAddress {
+  unsigned long long ctx_id;
+  int* ptr;
+};
 std::mutex g_scratch_mu;
-int* g_scratch_ptr[kMaxCachedDevices] = {};
+CachedAddress g_scratch_cache[kMaxCachedContexts] = {};
+int g_scratch_used = 0;
 
-// Device address of g_dispatch_scratch on the current device (looked up once per device).
-cudaError_t scratch_on_current_device(int** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+cudaError_t load_context_calls() {
+  if (g_ctx_get_current != nullptr && g_ctx_get_id != nullptr) return cudaSuccess;
+  void* f1 = nullptr;
+  void* f2 = nullptr;
+  cudaDriverEntryPointQueryResult q1, q2;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+  if (e != cudaSuccess || q1 != cudaDriverEntryPointSuccess || f1 == nullptr) return cudaErrorSymbolNotFound;
+  e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+  if (e != cudaSuccess || q2 != cudaDriverEntryPointSuccess || f2 == nullptr) return cudaErrorSymbolNotFound;
+  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  return cudaSuccess;
+}
+
+// Device address of g_dispatch_scratch in the current context (looked up
+// once per context, keyed by the context's process-unique id).
+cudaError_t scratch_in_current_context(int** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (dev >= 0 && dev < kMaxCachedDevices && g_scratch_ptr[dev] != nullptr) {
-    *out = g_scratch_ptr[dev];
-    return cudaSuccess;
-  }
-  void* p = nullptr;
-  e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+  cudaError_t e = load_context_calls();
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < kMaxCachedDevices) g_scratch_ptr[dev] = static_cast<int*>(p);
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  void* p = nullptr;
+  if (ctx == nullptr) {
+    // no context is current yet: the runtime creates the device's primary
+    // context for this lookup and makes it current
+    if ((e = cudaGetSymbolAddress(&p, g_dispatch_scratch)) != cudaSuccess) return e;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cudaErrorDeviceUninitialized;
+  }
+  unsigned long long id = 0;
+  if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+  for (int i = 0; i < g_scratch_used; ++i) {
+    if (g_scratch_cache[i].ctx_id == id) {
+      *out = g_scratch_cache[i].ptr;
+      return cudaSuccess;
+    }
+  }
+  if (p == nullptr && (e = cudaGetSymbolAddress(&p, g_dispatch_scratch)) != cudaSuccess) return e;
+  // a full table overwrites an entry (that context, if used again, is looked up again)
+  const int slot = g_scratch_used < kMaxCachedContexts ? g_scratch_used++ : static_cast<int>(id % kMaxCachedContexts);
+  g_scratch_cache[slot] = CachedAddress{id, static_cast<int*>(p)};
   *out = static_cast<int*>(p);
   return cudaSuccess;
 }
@@ -74,14 +116,12 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C
                                              const void* x, int32_t* pos, int32_t* counts, int32_t* offsets,
                                              int64_t* dropped, void* x_perm, int32_t* row_token,
                                              int32_t* error_out, void* stream) {
-  if (shape == nullptr || C < 0) return MOE_ERR_INVALID_ARG;
-  if (shape->T < 0 || shape->d < 1 || shape->E < 1 || shape->k < 1 || shape->k > shape->E ||
-      shape->d_ff < 1 || (shape->dtype != MOE_F32 && shape->dtype != MOE_BF16) ||
-      (shape->act != MOE_ACT_GELU && shape->act != MOE_ACT_SWIGLU))
-    return MOE_ERR_INVALID_ARG;
+  // the same shapes as moe_dispatch (an invalid or unsupported one returns before anything is enqueued)
+  const moe_status_t sst = check_shape(shape);
+  if (sst != MOE_OK) return sst;
+  if (C < 0) return MOE_ERR_INVALID_ARG;
   // the plain token-choice dispatch only: no expert choice, no re-routing pass
   if (shape->routing != MOE_ROUTE_TOKEN_CHOICE || shape->overflow != MOE_OVERFLOW_DROP) return MOE_ERR_INVALID_ARG;
-  if (shape->E > kMaxExperts || shape->k > kMaxTopK) return MOE_ERR_UNSUPPORTED;
   const long long Tk = shape->T * static_cast<long long>(shape->k);
   if (Tk > kNoAllocMaxAssignments) return MOE_ERR_UNSUPPORTED;  // beyond the fixed scratch array
   if (counts == nullptr || offsets == nullptr || dropped == nullptr) return MOE_ERR_INVALID_ARG;
@@ -89,9 +129,12 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_shape_t* shape, int32_t C
   const long long EC = static_cast<long long>(shape->E) * C;
   const long long rows = Tk < EC ? Tk : EC;
   if (rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  // the gather moves rows in 16-byte units
+  const auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
+  if ((shape->T > 0 && misaligned(x)) || (rows > 0 && misaligned(x_perm))) return MOE_ERR_UNSUPPORTED;
 
   int* scratch = nullptr;
-  if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  if (scratch_in_current_context(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (error_out != nullptr && cudaMemsetAsync(error_out, 0, sizeof(int32_t), st) != cudaSuccess)
     return MOE_ERR_CUDA;

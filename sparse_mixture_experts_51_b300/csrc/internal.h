@@ -107,6 +107,8 @@ inline int dispatch_nblk(long long Tk) {
 }
 
 WsLayout ws_layout(const moe_shape_t& s, int32_t C);
+// MOE_OK, or the status every entry point returns for an invalid or unsupported shape
+moe_status_t check_shape(const moe_shape_t* s);
 
 struct RouterParams {
   const void* x;

@@ -75,8 +75,7 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   return L;
 }
 
-namespace {
-
+// Argument check shared by every entry point that takes a layer shape.
 moe_status_t check_shape(const moe_shape_t* s) {
   if (s == nullptr) return MOE_ERR_INVALID_ARG;
   if (s->T < 0 || s->d < 1 || s->E < 1 || s->k < 1 || s->d_ff < 1) return MOE_ERR_INVALID_ARG;
@@ -98,6 +97,8 @@ moe_status_t check_shape(const moe_shape_t* s) {
     return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
+
+namespace {
 
 moe_status_t check_ws(const moe_shape_t* s, int32_t C, const void* ws, size_t ws_bytes) {
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return MOE_ERR_WORKSPACE;
@@ -369,6 +370,8 @@ moe_status_t moe_dispatch(const moe_shape_t* shape, int32_t C, const int32_t* id
   if (shape->T > 0 && (idx == nullptr || x == nullptr || pos == nullptr)) return MOE_ERR_INVALID_ARG;
   const WsLayout L = ws_layout(*shape, C);
   if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
+  // the gather moves rows in 16-byte units
+  if ((shape->T > 0 && !aligned16(x)) || (L.rows > 0 && !aligned16(x_perm))) return MOE_ERR_UNSUPPORTED;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
   return dispatch_impl(shape, C, const_cast<int32_t*>(idx), x, pos, counts, offsets, dropped, x_perm, row_token,
                        ws, L, static_cast<cudaStream_t>(stream));
@@ -387,6 +390,7 @@ moe_status_t moe_testing_dispatch_stalled(const moe_shape_t* shape, int32_t C, c
   const WsLayout L = ws_layout(*shape, C);
   if (L.rows > 0 && x_perm == nullptr) return MOE_ERR_INVALID_ARG;
   if (stalled_tile < 0 || stalled_tile >= L.nblk_dispatch) return MOE_ERR_INVALID_ARG;
+  if ((shape->T > 0 && !aligned16(x)) || (L.rows > 0 && !aligned16(x_perm))) return MOE_ERR_UNSUPPORTED;
   if ((st = check_ws(shape, C, ws, ws_bytes)) != MOE_OK) return st;
   return dispatch_impl(shape, C, const_cast<int32_t*>(idx), x, pos, counts, offsets, dropped, x_perm, nullptr, ws,
                        L, static_cast<cudaStream_t>(stream), stalled_tile);

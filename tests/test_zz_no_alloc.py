@@ -6,8 +6,12 @@ instead of a caller workspace; its results must equal moe_dispatch's.
 
 This file is collected last on purpose, and must pass both alone in a fresh
 process (the first call sets up the array's device address) and after the
-other GPU tests."""
+other GPU tests; test_noalloc_in_a_fresh_process runs the rest of the file
+in a new Python process to check the first."""
 import ctypes
+import os
+import subprocess
+import sys
 
 import pytest
 import torch
@@ -52,10 +56,15 @@ def _noalloc(shape, C, idx, x):
     return out
 
 
-@pytest.mark.parametrize("T,d,E,k,cf", [(3000, 128, 16, 2, 0.8), (700, 64, 8, 1, 1.0)])
+@pytest.mark.parametrize("T,d,E,k,cf", [(3000, 128, 16, 2, 0.8), (2600, 64, 8, 1, 1.0),
+                                         (MAX_ASSIGNMENTS // 2, 64, 8, 2, 0.9)],
+                         ids=["tiled_then_tiled", "tiled_then_one_cta", "256_large_tiles"])
 def test_noalloc_dispatch_matches_workspace_dispatch_twice(T, d, E, k, cf):
     """Two calls in a row (different batches, so the second starts from the
-    first call's leftover scratch) each equal the workspace entry point."""
+    first call's leftover scratch) each equal the workspace entry point.  The
+    cases cover the tiled look-back kernel (more than 2048 assignments) with
+    1024-assignment tiles, the one-CTA kernel, and the largest size the fixed
+    array holds: 2^20 assignments in 256 tiles of 4096."""
     for call, seed in enumerate((101, 202)):
         Tc = T if call == 0 else T // 2 + 1
         idx, x = _inputs(Tc, d, E, k, seed)
@@ -80,3 +89,35 @@ def test_noalloc_rejects_sizes_beyond_its_array():
     st = _lib.load().moe_dispatch_noalloc(ctypes.byref(shape), 10, _P(idx), _P(x), _P(idx), _P(idx), _P(idx),
                                           _P(idx), _P(x), None, None, None)
     assert st == 2  # MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_rejects_what_the_workspace_dispatch_rejects():
+    """Shapes and pointers that moe_dispatch refuses are refused here too,
+    before anything is enqueued: a bf16 width that is not a multiple of 64
+    and a token matrix that is not 16-byte aligned."""
+    idx, x = _inputs(64, 64, 4, 2, 8)
+    lib = _lib.load()
+    buf = torch.zeros(4096, dtype=torch.int32, device="cuda")
+    bad_d = api.shape_of(64, 33, 4, 2, 64, torch.bfloat16, "gelu")
+    st = lib.moe_dispatch_noalloc(ctypes.byref(bad_d), 40, _P(idx), _P(x), _P(buf), _P(buf), _P(buf), _P(buf),
+                                  _P(buf), None, None, None)
+    assert st == 2  # MOE_ERR_UNSUPPORTED
+    shape = api.shape_of(63, 64, 4, 2, 64, torch.bfloat16, "gelu")
+    x_odd = x.view(-1)[1:63 * 64 + 1]  # starts 2 bytes past an aligned address
+    st = lib.moe_dispatch_noalloc(ctypes.byref(shape), 40, _P(idx), ctypes.c_void_p(x_odd.data_ptr()), _P(buf),
+                                  _P(buf), _P(buf), _P(buf), _P(buf), None, None, None)
+    assert st == 2
+    ws = api.new_workspace(shape, 40)
+    st = lib.moe_dispatch(ctypes.byref(shape), 40, _P(idx), ctypes.c_void_p(x_odd.data_ptr()), _P(buf), _P(buf),
+                          _P(buf), _P(buf), _P(buf), None, _P(ws), ws.numel(), None)
+    assert st == 2
+
+
+def test_noalloc_in_a_fresh_process():
+    """The other tests of this file, alone in a new process: the first call
+    there finds the array's address itself."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-m", "gpu", "-p", "no:cacheprovider",
+                        "-k", "not fresh_process", os.path.abspath(__file__)],
+                       cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
