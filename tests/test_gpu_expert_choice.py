@@ -13,7 +13,7 @@ from oracle import moe_oracle as O
 from sparse_mixture_experts_51_b300 import api
 from sparse_mixture_experts_51_b300 import workloads as W
 
-from _parity import F64Experts, oracle_shared, rel_l2, shared_args, to_gpu, tolerance
+from _parity import F64Experts, check_rows, oracle_shared, rel_l2, segment_edge_rows, shared_args, to_gpu, tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -67,6 +67,9 @@ def check_ec(w, gpu, ref, tokens=None):
     e1 = rel_l2(gpu["moe"].numpy()[toks], ref["moe"])
     e2 = rel_l2(gpu["out"].float().numpy()[toks], ref["out"])
     assert e1 <= tol and e2 <= tol, (e1, e2)
+    # token by token as well
+    check_rows("moe", gpu["moe"].numpy()[toks], ref["moe"], tol, labels=toks)
+    check_rows("out", gpu["out"].float().numpy()[toks], ref["out"], tol, labels=toks)
 
 
 CASES = [
@@ -149,7 +152,12 @@ def test_full_size_switch_expert_choice_sampled():
     w = W.WORKLOADS["switch_top1"]
     inp = W.make_inputs(w)
     gpu = gpu_ec(w, to_gpu(inp))
-    toks = np.sort(np.random.default_rng(9).choice(w.T, size=64, replace=False))
+    toks = np.random.default_rng(9).choice(w.T, size=64, replace=False).tolist()
+    # the tokens on the edge rows of every expert's segment (rows e*C' .. e*C'+C'-1 hold sel[e])
+    Cp = min(gpu["C"], w.T)
+    sel = gpu["sel"].numpy().reshape(-1)
+    edges = segment_edge_rows(np.arange(w.E + 1) * Cp, head=2, tail=8)
+    toks = np.array(sorted(set(toks + sel[edges].tolist())))
     ref = oracle_ec(w, inp, tokens=toks)
     check_ec(w, gpu, ref, tokens=toks)
 

@@ -12,7 +12,7 @@ import torch
 
 from sparse_mixture_experts_51_b300 import workloads as W
 
-from _parity import check_layer, gpu_forward, oracle_forward, to_gpu
+from _parity import check_layer, edge_tokens, gpu_forward, oracle_forward, to_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -77,7 +77,8 @@ def test_full_size_switch_reroute_sampled():
     w = W.WORKLOADS["switch_top1"]
     inp = W.make_inputs(w)
     gpu = gpu_forward(w, to_gpu(inp), overflow="reroute")
-    toks = np.sort(np.random.default_rng(11).choice(w.T, size=64, replace=False))
+    toks = np.random.default_rng(11).choice(w.T, size=64, replace=False).tolist()
+    toks = np.array(sorted(set(toks + edge_tokens(gpu["idx"].numpy(), gpu["pos"].numpy(), gpu["offsets"].numpy()))))
     ref = oracle_forward(w, inp, tokens=toks, overflow="reroute")
     assert ref["rerouted"] > 0
     check_layer(w, inp, gpu, ref, tokens=toks)

@@ -13,7 +13,7 @@ from oracle import moe_oracle as O
 from sparse_mixture_experts_51_b300 import api
 from sparse_mixture_experts_51_b300 import workloads as W
 
-from _parity import check_layer, gpu_forward, oracle_forward, rel_l2, to_gpu
+from _parity import check_layer, edge_tokens, gpu_forward, oracle_forward, rel_l2, to_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -137,10 +137,17 @@ def test_full_size_decode_t128():
 
 
 def _sampled(w, n_sample=48):
+    """Routing, slots and drops for every token; outputs on a token sample
+    that holds, besides random tokens and the first and last eight, every
+    token with an assignment on an edge row of its expert's segment (first
+    and last rows, the rows of partial M tiles): the rows the expert GEMMs
+    store by their edge paths."""
     inp = W.make_inputs(w)
     gpu = gpu_forward(w, to_gpu(inp))
     rng = np.random.default_rng(w.seed)
-    toks = sorted(set(list(range(8)) + list(range(w.T - 8, w.T)) + rng.choice(w.T, n_sample, replace=False).tolist()))
+    edges = edge_tokens(gpu["idx"].numpy(), gpu["pos"].numpy(), gpu["offsets"].numpy())
+    toks = sorted(set(list(range(8)) + list(range(w.T - 8, w.T)) + rng.choice(w.T, n_sample, replace=False).tolist()
+                      + edges))
     ref = oracle_forward(w, inp, tokens=toks)
     check_layer(w, inp, gpu, ref, tokens=toks)
     return inp, gpu, ref

@@ -13,7 +13,8 @@ from oracle import moe_oracle as O
 from sparse_mixture_experts_51_b300 import api
 from sparse_mixture_experts_51_b300 import workloads as W
 
-from _parity import check_layer, gpu_forward, oracle_forward, oracle_shared, rel_l2, shared_args, to_gpu, tolerance
+from _parity import (check_layer, check_rows, edge_tokens, gpu_forward, oracle_forward, oracle_shared, rel_l2,
+                     shared_args, to_gpu, tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,6 +73,8 @@ def test_shared_ffn_alone(w):
     ref = O.shared_experts(W.as_f64_numpy(inp["x"]), w.act, sh["W1s"], sh["W2s"], sh["W3s"], sh["b1s"], sh["b2s"])
     err = rel_l2(y.cpu().numpy(), ref)
     assert err <= tolerance(w), err
+    # every token's row, the dense group's last (partial) M tile included
+    check_rows("shared", y.cpu().numpy(), ref, tolerance(w))
 
 
 def test_step_by_step_combine_with_shared_matches_forward():
@@ -92,6 +95,7 @@ def test_step_by_step_combine_with_shared_matches_forward():
     assert torch.equal(out.cpu(), full["out"])
     ref = oracle_forward(w, inp)
     assert rel_l2(moe.cpu().numpy(), ref["moe"]) <= tolerance(w)
+    check_rows("moe", moe.cpu().numpy(), ref["moe"], tolerance(w))
 
 
 def test_full_size_shared_layer_sampled():
@@ -102,7 +106,10 @@ def test_full_size_shared_layer_sampled():
     inp = W.make_inputs(w)
     gpu = gpu_forward(w, to_gpu(inp))
     rng = np.random.default_rng(7)
-    toks = np.sort(rng.choice(w.T, size=48, replace=False))
+    toks = rng.choice(w.T, size=48, replace=False).tolist()
+    # the tokens on each expert's segment edges (last 8 rows, partial tiles): 64 experts make this a large sample
+    toks += edge_tokens(gpu["idx"].numpy(), gpu["pos"].numpy(), gpu["offsets"].numpy(), head=1, tail=8)
+    toks = np.array(sorted(set(toks + list(range(w.T - 32, w.T)))))
     ref = oracle_forward(w, inp, tokens=toks)
     check_layer(w, inp, gpu, ref, tokens=toks)
 
