@@ -8,10 +8,18 @@ expert GEMMs, combine) over one batch of seeded synthetic tokens already
 resident in HBM, issued through the C ABI (moe_forward_timed).  The timed
 steps are replayed as CUDA graphs (--eager: launched from the host); L2 is
 flushed (256 MiB write) between timed steps, outside the measured events.
-Prints one JSON line.  Besides the layer, the line carries `routing_stats`:
-the time of one moe_routing_stats call over the same batch (routing
-diagnostics and auxiliary load-balancing loss; L2 flushed before each call)
-and the values it returned.
+
+Prints one JSON line for the headline layer (--workload, by default the
+Mixtral-shaped layer: T=16384, d=4096, E=8 top-2, SwiGLU d_ff=14336, no
+drops).  At one GPU the line also carries `per_config`: the same measurement
+(shorter) for each of the five layer configurations -- tiny fp32, bf16
+T=4096, Mixtral-shaped, Switch-style top-1 with forced overflow, and the
+decode-like T=128 layer -- each with its roofline (tensor TFLOP/s for the
+compute-bound shapes, HBM GB/s for the weight-streaming ones), near-tie and
+drop counts, end-to-end rate with host buffers, and the fp64 CPU oracle
+timed on the host cores (all threads, and one thread for the small layers).
+The line carries `routing_stats` too: one moe_routing_stats call over the
+same batch (routing diagnostics and the auxiliary load-balancing loss).
 
 --impl reference times the fp64 CPU oracle instead (the reference arm of this
 benchmark), on the host cores, each step a bounded sub-batch of the workload.
@@ -37,8 +45,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer fwd tokens/s on 1 B300; TFLOP/s or HBM GB/s as % of roofline"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "bf16_t4096"
+DEFAULT_WORKLOAD = "mixtral_t16384"
 FLUSH_BYTES = 256 << 20
+# the five layer configurations, in their usual order (each gets a per_config entry)
+PER_CONFIG = ["tiny_fp32", "bf16_t4096", "mixtral_t16384", "switch_top1", "decode_t128"]
+PER_CONFIG_STEPS = 200
+PER_CONFIG_E2E_STEPS = 40
+# layers whose oracle is also timed on one host thread
+SINGLE_THREAD_CPU = ("tiny_fp32", "bf16_t4096", "decode_t128")
+# the ~8 TB/s HBM figure the weight-streaming layer's bandwidth target is quoted against
+HBM_NOMINAL_GBS = 8000.0
 
 # DRAM traffic of the dominant kernel per launch, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
@@ -54,8 +70,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline sample budget of the headline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the headline layer only")
     ap.add_argument("--eager", action="store_true", help="launch every kernel from the host (no CUDA graph)")
     return ap.parse_args(argv)
 
@@ -88,18 +105,48 @@ def load_peaks():
     return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def gemm1_work(w, counts):
-    """Algorithmic flops and DRAM bytes of the first expert GEMM (dominant kernel)
-    for the kept rows: flops 2*d*F per row (x2 for SwiGLU's gate and up),
-    bytes = weights of every expert with a kept row + grouped rows read + hidden written."""
+def cpu_model() -> str:
+    """The host CPU's model name (as lscpu prints it)."""
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
+def layer_work(w, counts):
+    """Algorithmic work of one layer forward with the given kept counts per expert.
+
+    flops: per kept row 2*d*F per expert matrix (W1, W3 for SwiGLU, W2);
+    bytes: tokens read once, the weights of every expert with a kept row,
+    the output written, the noise table when noisy, and the routing tables
+    (idx, gates, slots: 12 bytes per assignment)."""
     from sparse_mixture_experts_51_b300 import workloads as W
     R = int(sum(counts))
     active = sum(1 for c in counts if c > 0)
     b = 2 if w.dtype_name == "bf16" else 4
-    mats = 2 if w.act == W.ACT_SWIGLU else 1
-    flops = float(R) * 2.0 * w.d * w.F * mats
-    nbytes = float(active) * mats * w.F * w.d * b + float(R) * w.d * b + float(R) * w.F * b
-    return flops, nbytes
+    mats1 = 2 if w.act == W.ACT_SWIGLU else 1
+    gemm1_flops = float(R) * 2.0 * w.d * w.F * mats1
+    ffn_flops = gemm1_flops + float(R) * 2.0 * w.d * w.F
+    weight_bytes = float(active) * (mats1 + 1) * w.F * w.d * b
+    layer_bytes = (2.0 * w.T * w.d * b + weight_bytes + (w.T * w.E * 4.0 if w.noisy else 0.0) + 12.0 * w.T * w.k)
+    gemm1_bytes = float(active) * mats1 * w.F * w.d * b + float(R) * w.d * b + float(R) * w.F * b
+    return dict(kept_rows=R, active_experts=active, gemm1_flops=gemm1_flops, ffn_flops=ffn_flops,
+                weight_bytes=weight_bytes, layer_bytes=layer_bytes, gemm1_bytes=gemm1_bytes)
+
+
+def recorded_traffic(name):
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as fh:
+        rec = json.load(fh).get(name)
+    if rec and rec.get("kernel_hash") == kernel_hash():
+        return rec.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
@@ -205,10 +252,11 @@ class ClockSampler:
 _ORACLE_CACHE = {}
 
 
-def cpu_oracle_run(w, budget_s: float):
+def cpu_oracle_run(w, budget_s: float, threads=None):
     """Time the fp64 oracle, as it stands, on a sub-batch of the workload (the
     same layer with its first T_s tokens as their own batch) for about
-    budget_s seconds.  Returns (tokens/s, sample description, threads, seconds)."""
+    budget_s seconds, on all host threads or on ``threads`` BLAS threads.
+    Returns (tokens/s, sample description, threads used, seconds)."""
     from oracle import moe_oracle as O
     from sparse_mixture_experts_51_b300 import workloads as W
 
@@ -222,11 +270,13 @@ def cpu_oracle_run(w, budget_s: float):
                 self.cache[e] = W.as_f64_numpy(self.t[e])
             return self.cache[e]
 
-    # sub-batch size from the algorithmic work per token (fp64 BLAS ~1e11 flop/s)
+    # sub-batch size from the algorithmic work per token (fp64 BLAS ~1e11 flop/s on all threads)
     per_tok = 2.0 * w.d * (3 if w.act == W.ACT_SWIGLU else 2) * (w.F * w.k + w.n_shared * w.F_shared) + 2.0 * w.d * w.E
-    T_s = int(max(16, min(w.T, budget_s * 1e11 / per_tok / 2)))
+    rate = 1e11 if threads is None else 5e9
+    T_s = int(max(16, min(w.T, budget_s * rate / per_tok / 2)))
     key = (w.name, T_s)
     if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE.clear()  # one workload's widened weights at a time
         inp = W.make_inputs(w.scaled(T_s))
         f = W.as_f64_numpy
         _ORACLE_CACHE[key] = (f(inp["x"]), f(inp["W_g"]), F64(inp["W1"]), F64(inp["W2"]), dict(
@@ -236,20 +286,34 @@ def cpu_oracle_run(w, budget_s: float):
             shared=None if inp["W1s"] is None else dict(
                 W1s=f(inp["W1s"]), W2s=f(inp["W2s"]), W3s=f(inp["W3s"]), b1s=f(inp["b1s"]), b2s=f(inp["b2s"]))))
     x, Wg, W1, W2, args = _ORACLE_CACHE[key]
-    runs, tokens, t0 = 0, 0, time.perf_counter()
-    while True:
+
+    def run():
         if w.routing == "expert":
             O.forward_expert_choice(x, Wg, w.act, W1, W2, k=w.k, **args)
         else:
             O.forward(x, Wg, w.k, w.act, W1, W2, **args)
-        runs += 1
-        tokens += T_s
-        el = time.perf_counter() - t0
-        if el >= budget_s or runs >= 1000:
-            break
-    cores = os.cpu_count()
+
+    limiter = None
+    if threads is not None:
+        from threadpoolctl import threadpool_limits
+        limiter = threadpool_limits(limits=threads)
+    try:
+        run()  # widens the expert weights to fp64 once (not timed)
+        runs, tokens, t0 = 0, 0, time.perf_counter()
+        while True:
+            run()
+            runs += 1
+            tokens += T_s
+            el = time.perf_counter() - t0
+            if el >= budget_s or runs >= 1000:
+                break
+    finally:
+        if limiter is not None:
+            limiter.unregister()
+    cores = os.cpu_count() if threads is None else threads
     sample = (f"{runs} oracle forward(s) of a {T_s}-token sub-batch of {w.name} (its own capacity "
-              f"ceil({w.capacity_factor}*{T_s}*{w.k}/{w.E})), fp64 NumPy, BLAS on all host threads")
+              f"ceil({w.capacity_factor}*{T_s}*{w.k}/{w.E})), fp64 NumPy, "
+              + ("BLAS on all host threads" if threads is None else f"BLAS on {threads} thread(s)"))
     return tokens / el, sample, cores, el
 
 
@@ -304,13 +368,15 @@ def run_reference(a):
             "warmup": a.warmup, "ms_per_step": 1e3 * total_t / a.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample,
+                             "cpu_model": cpu_model()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
 def workload_config(w):
+    """The workload as the JSON line's `config` (identical in both arms)."""
     from sparse_mixture_experts_51_b300 import workloads as W
     return {"workload": w.name, "T": w.T, "d": w.d, "E": w.E, "k": w.k, "d_ff": w.F,
             "act": "swiglu" if w.act == W.ACT_SWIGLU else "gelu", "capacity_factor": w.capacity_factor,
@@ -320,183 +386,195 @@ def workload_config(w):
             "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
 
 
-def run_ours(a):
-    import ctypes
+class DeviceLayer:
+    """One workload's layer resident on the GPU: inputs, weights, workspace and
+    the argument list of moe_forward / moe_forward_timed."""
+
+    def __init__(self, w, dev, lib, keep_host_tokens=True):
+        import ctypes
+
+        import torch
+
+        from sparse_mixture_experts_51_b300 import api
+        from sparse_mixture_experts_51_b300 import workloads as W
+
+        self.w, self.dev, self.lib = w, dev, lib
+        inp = W.make_inputs(w)
+        self.x_host = inp["x"] if keep_host_tokens else None
+        self.eps_host = inp["eps"] if keep_host_tokens else None
+        self.g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+        del inp
+        g = self.g
+        self.act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
+        self.C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
+        sw = W.shared_wide(g)
+        self.Fsh = 0 if sw["W1s"] is None else sw["W1s"].shape[0]
+        self.shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, self.act, d_ff_shared=self.Fsh,
+                                  routing=w.routing)
+        self.shared_t = None
+        self.shared_w = None
+        if self.Fsh:
+            b2s = None if sw["b2s_rows"] is None else sw["b2s_rows"].sum(dim=0).contiguous()
+            self.shared_t = dict(W1s=sw["W1s"], W2s=sw["W2s"], W3s=sw["W3s"], b1s=sw["b1s"], b2s=b2s)
+            self.shared_w = api.shared_weights(**self.shared_t)
+        self.shared_arg = ctypes.addressof(self.shared_w) if self.shared_w is not None else None
+        self.ws = api.new_workspace(self.shape, self.C, dev)
+        self.out = torch.empty(w.T, w.d, dtype=w.dtype, device=dev)
+        self.counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+        self.dropped = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def args(self, stats=None, idx=None, logits=None):
+        import ctypes
+
+        import torch
+
+        from sparse_mixture_experts_51_b300 import api
+        P, g, w = api._ptr, self.g, self.w
+        # the stream current at the call (the capture stream while a graph is recorded)
+        sptr = ctypes.c_void_p(torch.cuda.current_stream(self.dev).cuda_stream)
+        return [ctypes.byref(self.shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
+                P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]),
+                self.shared_arg, P(self.out), None, P(idx), None, None, P(self.counts), None, P(self.dropped),
+                P(stats), P(logits), P(self.ws), self.ws.numel(), sptr]
+
+    def forward(self, **kw):
+        from sparse_mixture_experts_51_b300 import _lib
+        _lib.check(self.lib.moe_forward(*self.args(**kw)), "moe_forward")
+
+    def forward_timed(self, events):
+        import ctypes
+
+        from sparse_mixture_experts_51_b300 import _lib
+        arr = (ctypes.c_void_p * 6)(*[None if e is None else ctypes.c_void_p(e.cuda_event) for e in events])
+        _lib.check(self.lib.moe_forward_timed(*self.args(), arr), "moe_forward_timed")
+
+    def device_error(self):
+        from sparse_mixture_experts_51_b300 import api
+        return api.get_device_error(self.ws)
+
+
+# events of the headline timing: before the router, around expert GEMM 1 (the
+# roofline kernel) and after the combine; none inside the router -> dispatch
+# -> gather and GEMM 2 -> combine chains, whose kernels overlap their
+# neighbours' tails through programmatic dependent launch
+TIMED_SLOTS = (0, 2, 3, 5)
+SPANS = {"router_dispatch_gather": (0, 2), "expert_gemm1": (2, 3), "expert_gemm2_combine": (3, 5)}
+# the per-stage split takes every event (which cuts the overlap between stages)
+STAGE_SPANS = {"router": (0, 1), "dispatch_gather": (1, 2), "expert_gemm1": (2, 3), "expert_gemm2": (3, 4),
+               "combine": (4, 5)}
+GRAPH_STEPS = 250
+
+
+def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=SPANS, sampler=None, barrier=None):
+    """Time ``steps`` layer forwards (moe_forward_timed; CUDA graphs of up to
+    GRAPH_STEPS steps, the L2 flush before each step outside its events).
+    Returns per-step device times (ms) and the per-step span times."""
+    import contextlib
 
     import torch
-    import torch.distributed as dist
-
-    from sparse_mixture_experts_51_b300 import _lib, api
-    from sparse_mixture_experts_51_b300 import workloads as W
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    dev = torch.device("cuda", local)
-    lib = _lib.load()
-
-    w = replica_workload(W.WORKLOADS[a.workload], rank, world)
-    inp = W.make_inputs(w)
-    g = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
-    act = "swiglu" if w.act == W.ACT_SWIGLU else "gelu"
-    C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
-    sw = W.shared_wide(g)
-    Fsh = 0 if sw["W1s"] is None else sw["W1s"].shape[0]
-    shape = api.shape_of(w.T, w.d, w.E, w.k, w.F, w.dtype, act, d_ff_shared=Fsh, routing=w.routing)
-    shared_w = None
-    if Fsh:
-        b2s = None if sw["b2s_rows"] is None else sw["b2s_rows"].sum(dim=0).contiguous()
-        shared_t = dict(W1s=sw["W1s"], W2s=sw["W2s"], W3s=sw["W3s"], b1s=sw["b1s"], b2s=b2s)
-        shared_w = api.shared_weights(**shared_t)
-    shared_arg = ctypes.addressof(shared_w) if shared_w is not None else None
-    ws = api.new_workspace(shape, C, dev)
-    out = torch.empty(w.T, w.d, dtype=w.dtype, device=dev)
-    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
-    dropped = torch.empty(1, dtype=torch.int64, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    P = api._ptr
-
-    def fwd_args():
-        # the stream current at the call (the capture stream while a graph is recorded)
-        sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-        return [ctypes.byref(shape), float(w.capacity_factor), -1, P(g["x"]), P(g["W_g"]), P(g["b_g"]),
-                P(g["W_noise"]), P(g["eps"]), P(g["W1"]), P(g["W3"]), P(g["W2"]), P(g["b1"]), P(g["b2"]), shared_arg,
-                P(out), None, None, None, None, P(counts), None, P(dropped), None, None, P(ws), ws.numel(), sptr]
-
-    # the timed steps run as CUDA graphs of up to GRAPH_STEPS steps each (every
-    # step the same C-ABI call, moe_forward_timed, its launches replayed
-    # without host gaps); the L2 flush between steps lies outside each
-    # step's events, and the events of a graph are read after each replay
-    GRAPH_STEPS = 250
-    G = min(a.steps, GRAPH_STEPS)
-    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(G)]
-
-    # events before the router, around expert GEMM 1 (the roofline kernel) and
-    # after the combine; none inside the router -> dispatch -> gather and
-    # GEMM 2 -> combine chains, whose kernels overlap their neighbours'
-    # tails through programmatic dependent launch
-    def step_timed(i):
-        evs = stage_ev[i]
-        arr = (ctypes.c_void_p * 6)(ctypes.c_void_p(evs[0].cuda_event), None, ctypes.c_void_p(evs[2].cuda_event),
-                                    ctypes.c_void_p(evs[3].cuda_event), None, ctypes.c_void_p(evs[5].cuda_event))
-        _lib.check(lib.moe_forward_timed(*fwd_args(), arr), "moe_forward_timed")
-
-    # make sure every event exists on the device before its handle is used
-    for evs in stage_ev:
-        for e in evs:
-            e.record(stream)
-    torch.cuda.synchronize()
-
-    for _ in range(a.warmup):
-        _lib.check(lib.moe_forward(*fwd_args()), "moe_forward")
-        flush.zero_()
-    torch.cuda.synchronize()
-    assert api.get_device_error(ws) == 0
-    # kernels one step enqueues (the library counts its own launches; a graph
-    # replays exactly what one captured call enqueued)
-    n0 = lib.moe_kernel_launches()
-    _lib.check(lib.moe_forward(*fwd_args()), "moe_forward")
-    kernels_per_step = int(lib.moe_kernel_launches() - n0)
+    G = min(steps, GRAPH_STEPS)
+    evs = [[torch.cuda.Event(enable_timing=True) if i in slots else None for i in range(6)] for _ in range(G)]
+    stream = torch.cuda.current_stream(L.dev)
+    # every event exists on the device before its handle is used
+    for row in evs:
+        for e in row:
+            if e is not None:
+                e.record(stream)
     torch.cuda.synchronize()
 
     graphs = {}
-
-    def graph_of(n):
-        if n not in graphs:
+    chunks = [G] * (steps // G) + ([steps % G] if steps % G else [])
+    if not eager:
+        for n in set(chunks):
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr):
                 for i in range(n):
                     flush.zero_()
-                    step_timed(i)
+                    L.forward_timed(evs[i])
             torch.cuda.synchronize()
             graphs[n] = gr
-        return graphs[n]
 
-    chunks = [G] * (a.steps // G) + ([a.steps % G] if a.steps % G else [])
-    if not a.eager:
-        for n in set(chunks):
-            graph_of(n)
-
-    step_ms, stage_ms = [], [[] for _ in range(3)]
-    SPANS = [(0, 2), (2, 3), (3, 5)]  # router+dispatch+gather, expert GEMM 1, expert GEMM 2+combine
-    sampler = ClockSampler(local)
-    with sampler:
-        sampler.wait_started()
-        if world > 1:
-            dist.barrier()
+    step_ms, span_ms = [], {k: [] for k in spans}
+    with (sampler if sampler is not None else contextlib.nullcontext()):
+        if sampler is not None:
+            sampler.wait_started()
+        if barrier is not None:
+            barrier()
         torch.cuda.synchronize()
         for n in chunks:
-            if a.eager:
+            if eager:
                 for i in range(n):
                     flush.zero_()
-                    step_timed(i)
+                    L.forward_timed(evs[i])
             else:
                 graphs[n].replay()
             torch.cuda.synchronize()
-            step_ms += [evs[0].elapsed_time(evs[5]) for evs in stage_ev[:n]]
-            for j, (u, v) in enumerate(SPANS):
-                stage_ms[j] += [evs[u].elapsed_time(evs[v]) for evs in stage_ev[:n]]
-        if world > 1:
-            dist.barrier()
+            step_ms += [row[slots[0]].elapsed_time(row[slots[-1]]) for row in evs[:n]]
+            for k, (u, v) in spans.items():
+                span_ms[k] += [row[u].elapsed_time(row[v]) for row in evs[:n]]
+        if barrier is not None:
+            barrier()
         torch.cuda.synchronize()
-    err = api.get_device_error(ws)
-    if err != 0:
-        raise RuntimeError(f"device-side error {err} during the timed region")
+    return step_ms, span_ms
 
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    value = job_throughput(w.T, a.steps, world, total_ms)
 
-    # ---------------- roofline of the dominant kernel (first expert GEMM)
-    cnt = counts.cpu().tolist()
-    flops, nbytes = gemm1_work(w, cnt)
-    g1_ms = statistics.mean(stage_ms[1])
-    peaks = load_peaks()
+def roofline_of(L, work, gemm1_ms, step_ms_mean, peaks, long_run):
+    """Roofline of the layer's dominant work.  Compute-bound shapes: expert
+    GEMM 1's TFLOP/s against the measured bf16 peak (the sustained figure when
+    the timed run is long enough for the power cap to set the clock, the burst
+    figure otherwise; both fractions are given).  Weight-streaming shapes: the
+    whole step's algorithmic HBM bytes over the step time against the measured
+    copy bandwidth and the nominal ~8 TB/s."""
+    w = L.w
+    traffic = recorded_traffic(w.name)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        with open(TRAFFIC_FILE) as fh:
-            rec = json.load(fh).get(w.name)
-        if rec and rec.get("kernel_hash") == kernel_hash():
-            traffic = rec.get("dram_bytes_per_launch")
-    if flops / nbytes >= ridge:
-        achieved = flops / (g1_ms / 1e3) / 1e12
-        roof = {"kernel": "grouped_gemm_kernel (expert GEMM 1, fused activation)", "bound": "tensor",
-                "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "peak_source": peaks["source"] + " bf16 burst",
-                "algorithmic_flops": flops, "ms_per_launch": g1_ms, "traffic": traffic}
-    else:
-        achieved = nbytes / (g1_ms / 1e3) / 1e9
-        roof = {"kernel": "grouped_gemm_kernel (expert GEMM 1, fused activation)", "bound": "hbm",
-                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"], "peak_source": peaks["source"] + " copy bandwidth",
-                "algorithmic_bytes": nbytes, "ms_per_launch": g1_ms, "traffic": traffic}
+    kernel = "grouped_gemm_kernel (expert GEMM 1, fused activation)"
+    if w.dtype_name != "bf16":
+        return {"kernel": "whole layer (fp32 CUDA-core path)", "bound": "latency", "achieved": step_ms_mean * 1e3,
+                "unit": "us/step", "peak": None, "frac": None,
+                "note": "a 64-token fp32 layer: six launches of a few microseconds each, no roofline applies"}
+    if work["gemm1_flops"] / work["gemm1_bytes"] >= ridge:
+        ach = work["gemm1_flops"] / (gemm1_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"] if long_run else peaks["bf16_tflops"]
+        return {"kernel": kernel, "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "peak_source": peaks["source"] + (" bf16 sustained" if long_run else " bf16 burst"),
+                "frac_of_burst": ach / peaks["bf16_tflops"], "frac_of_sustained": ach / peaks["bf16_tflops_sustained"],
+                "algorithmic_flops": work["gemm1_flops"], "ms_per_launch": gemm1_ms, "traffic": traffic,
+                "layer_tflops": work["ffn_flops"] / (step_ms_mean / 1e3) / 1e12}
+    ach = work["layer_bytes"] / (step_ms_mean / 1e3) / 1e9
+    return {"kernel": "whole step (expert weight stream: both expert GEMMs)", "bound": "hbm", "achieved": ach,
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+            "peak_source": peaks["source"] + " copy bandwidth", "frac_of_nominal_8tbs": ach / HBM_NOMINAL_GBS,
+            "algorithmic_bytes": work["layer_bytes"], "weight_bytes": work["weight_bytes"],
+            "gemm1_gbs": work["gemm1_bytes"] / (gemm1_ms / 1e3) / 1e9, "gemm1_ms": gemm1_ms, "traffic": traffic}
 
-    # ---------------- end to end through the public API with host buffers.
-    # Every step copies its tokens (and noise) from pinned host memory, runs
-    # the layer (MoELayer, the public call) and reads the output back to
-    # pinned host memory.  Like a serving loop the steps are pipelined on
-    # three streams with two device buffer sets: the input copy of step i+1
-    # and the output copy of step i-1 overlap the layer of step i.  The timed
-    # region spans the first input copy to the last output copy; no L2 flush
-    # (every step's inputs arrive from the host, and the expert weights are
-    # read from HBM each step).
-    layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
+
+def e2e_of(L, n_steps, warmup, world=1):
+    """End to end through the public API (MoELayer) with host buffers: every
+    step copies its tokens (and noise) from pinned host memory, runs the layer
+    and reads the output back to pinned host memory.  Like a serving loop the
+    steps are pipelined on three streams with two device buffer sets: the
+    input copy of step i+1 and the output copy of step i-1 overlap the layer
+    of step i.  The timed region spans the first input copy to the last
+    output copy; no L2 flush (every step's inputs arrive from the host, and
+    the expert weights are read from HBM each step)."""
+    import torch
+
+    from sparse_mixture_experts_51_b300 import api
+    w, g, dev = L.w, L.g, L.dev
+    stream = torch.cuda.current_stream(dev)
+    layer = api.MoELayer(g["W_g"], g["W1"], g["W2"], w.k, L.act, W3=g["W3"], b_g=g["b_g"], W_noise=g["W_noise"],
                          b1=g["b1"], b2=g["b2"], capacity_factor=w.capacity_factor, keep_routing=False,
-                         routing=w.routing, **(shared_t if Fsh else {}))
-    x_host = inp["x"].pin_memory()
-    eps_host = inp["eps"].pin_memory() if inp["eps"] is not None else None
+                         routing=w.routing, **(L.shared_t or {}))
+    x_host = L.x_host.pin_memory()
+    eps_host = L.eps_host.pin_memory() if L.eps_host is not None else None
     out_host = [torch.empty(w.T, w.d, dtype=w.dtype).pin_memory() for _ in range(2)]
     x_dev = [torch.empty_like(g["x"]) for _ in range(2)]
     eps_dev = [torch.empty_like(g["eps"]) if g["eps"] is not None else None for _ in range(2)]
-    out_dev = [torch.empty_like(out) for _ in range(2)]
+    out_dev = [torch.empty_like(L.out) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-    def e2e_run(n):
-        """n pipelined steps; returns the elapsed ms from the first input copy to the last output copy."""
+    def run(n):
         ev = lambda: torch.cuda.Event(enable_timing=False)
         in_ready, comp_done, out_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -527,94 +605,225 @@ def run_ours(a):
         torch.cuda.synchronize()
         return t0.elapsed_time(t1)
 
-    e2e_run(max(2, a.warmup))
-    n_e2e = max(2, a.steps)
-    e2e_ms = max_over_ranks(e2e_run(n_e2e), world, dev)
+    run(max(2, warmup))
+    n = max(2, n_steps)
+    ms = max_over_ranks(run(n), world, dev)
     # the layer run through the public call gives the device-timed output, bit for bit
-    if not torch.equal(out_host[(n_e2e - 1) % 2], out.cpu()):
-        raise RuntimeError("end-to-end output differs from the timed layer's output")
+    if not torch.equal(out_host[(n - 1) % 2], L.out.cpu()):
+        raise RuntimeError(f"{w.name}: end-to-end output differs from the timed layer's output")
     h2d = x_host.numel() * x_host.element_size() + (eps_host.numel() * 4 if eps_host is not None else 0)
     d2h = out_host[0].numel() * out_host[0].element_size()
-    e2e = {"value": job_throughput(w.T, n_e2e, world, e2e_ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "pipelined": "input copy of step i+1 and output copy of step i-1 overlap "
-                                                   "the layer of step i (two buffer sets, three streams)"}
+    # the host link alone: the same input copy, back to back, timed on its own
+    link = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(s_in):
+        x_dev[0].copy_(x_host, non_blocking=True)
+        link[0].record(s_in)
+        for _ in range(5):
+            x_dev[0].copy_(x_host, non_blocking=True)
+        link[1].record(s_in)
+    torch.cuda.synchronize()
+    link_gbs = 5 * x_host.numel() * x_host.element_size() / (link[0].elapsed_time(link[1]) / 1e3) / 1e9
+    return {"value": job_throughput(w.T, n, world, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n, "ms_per_step": ms / n,
+            "h2d_gbs_achieved": h2d * n / (ms / 1e3) / 1e9, "h2d_gbs_link": link_gbs,
+            "pipelined": "input copy of step i+1 and output copy of step i-1 overlap the layer of step i "
+                         "(two buffer sets, three streams)"}
 
-    # ---------------- routing diagnostics + aux loss of the same batch (moe_routing_stats,
-    # a separate call after the layer; token-choice routing only, it needs a top-k table)
-    routing_stats = None
+
+def routing_counts(L):
+    """One forward with the routing statistics on: [fp64-re-evaluated tokens,
+    near-tie tokens (k-th and (k+1)-th logits within 1e-4)], the kept rows per
+    expert and the drop count."""
+    import torch
+    if L.w.routing != "token":
+        L.forward()
+        torch.cuda.synchronize()
+        return None, L.counts.cpu().tolist(), int(L.dropped.item())
+    stats = torch.zeros(2, dtype=torch.int64, device=L.dev)
+    L.forward(stats=stats)
+    torch.cuda.synchronize()
+    st = stats.cpu().tolist()
+    return {"fp64_reevaluated_tokens": st[0], "near_tie_tokens": st[1],
+            "near_tie_rule": "k-th and (k+1)-th fp32 logits within 1e-4 (routing is exact for them too: "
+                             "the router certifies its order and re-evaluates unsettled tokens in fp64)"}, \
+        L.counts.cpu().tolist(), int(L.dropped.item())
+
+
+def routing_stats_of(L, peaks):
+    """moe_routing_stats (routing diagnostics + aux loss) over the layer's
+    batch, timed as a CUDA graph of back-to-back calls: the call follows the
+    layer, whose router has just written the logits, so its inputs are
+    L2-resident."""
+    import ctypes
+
+    import torch
+
+    from sparse_mixture_experts_51_b300 import _lib, api
+    w, dev, lib = L.w, L.dev, L.lib
+    if w.routing != "token":
+        return None
+    P = api._ptr
+    logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
+    idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+    L.forward(idx=idx_t, logits=logits)
+    st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
+
+    def call():
+        sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+        _lib.check(lib.moe_routing_stats(ctypes.byref(L.shape), P(logits), P(idx_t), P(L.counts), P(L.dropped),
+                                         P(st_out[0]), P(st_out[1]), P(st_out[2]), P(L.ws), L.ws.numel(), sptr),
+                   "moe_routing_stats")
+
     n_st = 50
-    sptr = ctypes.c_void_p(stream.cuda_stream)
-    if w.routing == "token":
-        logits = torch.empty(w.T, w.E, dtype=torch.float32, device=dev)
-        idx_t = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
-        fa = fwd_args()
-        fa[16], fa[23] = P(idx_t), P(logits)
-        _lib.check(lib.moe_forward(*fa), "moe_forward")
-        st_out = [torch.empty(n, dtype=torch.float64, device=dev) for n in (w.E, w.E, len(api.STATS_SUMMARY))]
-        sptr = ctypes.c_void_p(stream.cuda_stream)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    gst = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gst):
+        for _ in range(n_st):
+            call()
+    stream = torch.cuda.current_stream(dev)
+    gst.replay()
+    sev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    sev[0].record(stream)
+    gst.replay()
+    sev[1].record(stream)
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise RuntimeError("device-side error in moe_routing_stats")
+    st_ms = sev[0].elapsed_time(sev[1]) / n_st
+    st_bytes = w.T * w.E * 4 + w.T * w.k * 4  # logits + top-k table, read once
+    summ = dict(zip(api.STATS_SUMMARY, st_out[2].tolist()))
+    return {"us_per_call": st_ms * 1e3, "timing": f"CUDA graph of {n_st} back-to-back calls, inputs L2-resident",
+            "algorithmic_bytes": st_bytes, "achieved_gbs": st_bytes / (st_ms / 1e3) / 1e9,
+            "frac_hbm": st_bytes / (st_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
+            "overflow": summ["overflow"]}
 
-        def stats_call():
-            _lib.check(lib.moe_routing_stats(ctypes.byref(shape), P(logits), P(idx_t), P(counts), P(dropped),
-                                             P(st_out[0]), P(st_out[1]), P(st_out[2]), P(ws), ws.numel(), sptr),
-                       "moe_routing_stats")
 
-        for _ in range(3):
-            stats_call()
-        # the call follows the layer, whose router has just written the logits,
-        # so its inputs are L2-resident: time a CUDA graph of n_st back-to-back
-        # calls (no host gaps between launches), after a warm-up replay
-        torch.cuda.synchronize()
-        gst = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gst):
-            sptr = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
-            for _ in range(n_st):
-                stats_call()
-        sptr = ctypes.c_void_p(stream.cuda_stream)
-        gst.replay()
-        sev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-        sev[0].record(stream)
-        gst.replay()
-        sev[1].record(stream)
-        torch.cuda.synchronize()
-        if api.get_device_error(ws) != 0:
-            raise RuntimeError("device-side error in moe_routing_stats")
-        st_ms = sev[0].elapsed_time(sev[1]) / n_st
-        st_bytes = w.T * w.E * 4 + w.T * w.k * 4  # logits + top-k table, read once
-        summ = dict(zip(api.STATS_SUMMARY, st_out[2].tolist()))
-        routing_stats = {"us_per_call": st_ms * 1e3, "timing": f"CUDA graph of {n_st} back-to-back calls, inputs L2-resident",
-                         "algorithmic_bytes": st_bytes,
-                         "achieved_gbs": st_bytes / (st_ms / 1e3) / 1e9,
-                         "frac_hbm": st_bytes / (st_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                         "aux_loss": summ["aux_loss"], "entropy": summ["entropy"], "load_cv": summ["load_cv"],
-                         "overflow": summ["overflow"]}
+def shared_ffn_of(L, flush, peaks):
+    """The shared experts alone (moe_shared_ffn: two dense GEMMs over every
+    token), kernel time with L2 flushed before each call."""
+    import ctypes
 
-    # ---------------- the shared experts alone (moe_shared_ffn: two dense GEMMs over
-    # every token), kernel time with L2 flushed before each call
-    shared_ffn = None
-    if Fsh:
-        y_sh = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+    import torch
 
-        def shared_call():
-            _lib.check(lib.moe_shared_ffn(ctypes.byref(shape), P(g["x"]), shared_arg, P(y_sh), P(ws), ws.numel(),
-                                          sptr), "moe_shared_ffn")
+    from sparse_mixture_experts_51_b300 import _lib, api
+    from sparse_mixture_experts_51_b300 import workloads as W
+    if not L.Fsh:
+        return None
+    w, dev, P = L.w, L.dev, api._ptr
+    y_sh = torch.empty(w.T, w.d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
 
-        for _ in range(3):
-            shared_call()
-        hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_st)]
-        for i in range(n_st):
-            flush.zero_()
-            hev[i][0].record(stream)
-            shared_call()
-            hev[i][1].record(stream)
-        torch.cuda.synchronize()
-        if api.get_device_error(ws) != 0:
-            raise RuntimeError("device-side error in moe_shared_ffn")
-        sh_ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in hev)
-        sh_flops = 2.0 * w.T * w.d * Fsh * ((2 if w.act == W.ACT_SWIGLU else 1) + 1)
-        shared_ffn = {"us_per_call": sh_ms * 1e3, "algorithmic_flops": sh_flops,
-                      "achieved_tflops": sh_flops / (sh_ms / 1e3) / 1e12,
-                      "frac_bf16": sh_flops / (sh_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                      "peak_source": peaks["source"] + " bf16 burst", "launches_per_call": 2}
+    def call():
+        _lib.check(L.lib.moe_shared_ffn(ctypes.byref(L.shape), P(L.g["x"]), L.shared_arg, P(y_sh), P(L.ws),
+                                        L.ws.numel(), ctypes.c_void_p(stream.cuda_stream)), "moe_shared_ffn")
+
+    for _ in range(3):
+        call()
+    n = 50
+    hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        hev[i][0].record(stream)
+        call()
+        hev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise RuntimeError("device-side error in moe_shared_ffn")
+    ms = statistics.mean(s_.elapsed_time(e_) for s_, e_ in hev)
+    flops = 2.0 * w.T * w.d * L.Fsh * ((2 if w.act == W.ACT_SWIGLU else 1) + 1)
+    return {"us_per_call": ms * 1e3, "algorithmic_flops": flops, "achieved_tflops": flops / (ms / 1e3) / 1e12,
+            "frac_bf16": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+            "peak_source": peaks["source"] + " bf16 burst", "launches_per_call": 2}
+
+
+def cpu_baselines(w, budget_s, single_thread):
+    """The oracle on all host threads (and on one thread for small layers)."""
+    v, sample, cores, _ = cpu_oracle_run(w, budget_s)
+    out = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample, "cpu_model": cpu_model()}
+    if single_thread:
+        v1, sample1, _, _ = cpu_oracle_run(w, budget_s, threads=1)
+        out["single_thread"] = {"value": v1, "unit": UNIT, "cores": 1, "sample": sample1}
+    return out
+
+
+def measure(L, a, flush, peaks, steps, e2e_steps, world=1, sampler_index=0, barrier=None):
+    """Everything the JSON line reports about one layer."""
+    import torch
+    w = L.w
+    for _ in range(max(3, a.warmup)):
+        L.forward()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise RuntimeError(f"{w.name}: device-side error in the warm-up")
+    # kernels one step enqueues (the library counts its own launches; a graph
+    # replays exactly what one captured call enqueued)
+    n0 = L.lib.moe_kernel_launches()
+    L.forward()
+    kernels_per_step = int(L.lib.moe_kernel_launches() - n0)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(sampler_index)
+    step_ms, span_ms = time_steps(L, steps, flush, eager=a.eager, sampler=sampler, barrier=barrier)
+    if L.device_error() != 0:
+        raise RuntimeError(f"{w.name}: device-side error during the timed region")
+    total_ms = max_over_ranks(sum(step_ms), world, L.dev)
+    # the per-stage split, every stage event recorded (outside the timed region)
+    _, stage = time_steps(L, min(steps, 20), flush, eager=a.eager, slots=tuple(range(6)), spans=STAGE_SPANS)
+    routing, counts, dropped = routing_counts(L)
+    work = layer_work(w, counts)
+    mean_step = total_ms / steps
+    gemm1_ms = statistics.mean(span_ms["expert_gemm1"])
+    long_run = total_ms >= 1000.0
+    res = {
+        "value": job_throughput(w.T, steps, world, total_ms), "ms_per_step": mean_step, "steps": steps,
+        "step_ms_quantiles": step_quantiles(step_ms),
+        "stage_ms": {k: statistics.mean(v) for k, v in span_ms.items()},
+        "stage_split_ms": {k: statistics.mean(v) for k, v in stage.items()},
+        "stage_split_note": "every stage event recorded: no programmatic-launch overlap across the stage borders",
+        "roofline": roofline_of(L, work, gemm1_ms, mean_step, peaks, long_run),
+        "gpu_launches": kernels_per_step * steps, "kernels_per_step": kernels_per_step,
+        "clocks": sampler.summary(),
+        "run": {"C": L.C, "kept_rows": work["kept_rows"], "active_experts": work["active_experts"],
+                "dropped": dropped, "parallelism": "replicas" if world > 1 else "single_gpu",
+                "launch": "eager" if a.eager else f"CUDA graphs of up to {GRAPH_STEPS} timed steps "
+                                                  "(moe_forward_timed each)"},
+        "routing": routing,
+        "e2e": e2e_of(L, e2e_steps, a.warmup, world),
+    }
+    return res
+
+
+def run_ours(a):
+    import torch
+    import torch.distributed as dist
+
+    from sparse_mixture_experts_51_b300 import _lib
+    from sparse_mixture_experts_51_b300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    lib = _lib.load()
+    peaks = load_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    w = replica_workload(W.WORKLOADS[a.workload], rank, world)
+    L = DeviceLayer(w, dev, lib)
+    m = measure(L, a, flush, peaks, a.steps, max(2, a.steps), world, local,
+                barrier=(dist.barrier if world > 1 else None))
+    routing_stats = routing_stats_of(L, peaks)
+    shared_ffn = shared_ffn_of(L, flush, peaks)
+    head_out = L.out  # kept for nothing beyond this point
+    del L, head_out
+    torch.cuda.empty_cache()
 
     if rank != 0:
         if world > 1:
@@ -624,26 +833,46 @@ def run_ours(a):
 
     cpu = None
     if not a.no_cpu_baseline and world == 1:
-        v, sample, cores, _ = cpu_oracle_run(w, a.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        cpu = cpu_baselines(w, a.cpu_seconds, single_thread=w.name in SINGLE_THREAD_CPU)
 
-    cfg = workload_config(w)
-    cfg.update({"C": C, "kept_rows": int(sum(cnt)), "dropped": int(dropped.item()),
-                "parallelism": "replicas" if world > 1 else "single_gpu",
-                "launch": "eager" if a.eager else f"CUDA graphs of up to {GRAPH_STEPS} timed steps (moe_forward_timed each)"})
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
-            "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "step_ms_quantiles": step_quantiles(step_ms),
-            "dtype": w.dtype_name, "data": "synthetic", "config": cfg,
-            "stage_ms": {n: statistics.mean(v) for n, v in zip(
-                [("shared_ffn_" if Fsh else "") + ("router_select_gather" if w.routing == "expert"
-                                                     else "router_dispatch_gather"), "expert_gemm1",
-                 "expert_gemm2_combine"], stage_ms)},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": kernels_per_step * a.steps,
-            "clocks": sampler.summary(), "routing_stats": routing_stats}
+    # ---------------- every layer configuration, one at a time (one GPU only)
+    per_config = None
+    if world == 1 and not a.no_per_config and a.workload in PER_CONFIG:
+        per_config = {}
+        for name in PER_CONFIG:
+            if name == a.workload:
+                entry = {k: m[k] for k in ("value", "ms_per_step", "steps", "step_ms_quantiles", "stage_ms",
+                                           "stage_split_ms", "roofline", "gpu_launches", "clocks", "run",
+                                           "routing", "e2e")}
+                entry["cpu_baseline"] = cpu
+            else:
+                wc = W.WORKLOADS[name]
+                Lc = DeviceLayer(wc, dev, lib)
+                mc = measure(Lc, a, flush, peaks, min(a.steps, PER_CONFIG_STEPS),
+                             min(max(2, a.steps), PER_CONFIG_E2E_STEPS), 1, local)
+                del Lc
+                torch.cuda.empty_cache()
+                entry = {k: mc[k] for k in ("value", "ms_per_step", "steps", "step_ms_quantiles", "stage_ms",
+                                            "stage_split_ms", "roofline", "gpu_launches", "clocks", "run",
+                                            "routing", "e2e")}
+                entry["cpu_baseline"] = (None if a.no_cpu_baseline else
+                                         cpu_baselines(wc, 3.0, single_thread=name in SINGLE_THREAD_CPU))
+            entry["unit"] = UNIT
+            entry["us_per_step"] = entry["ms_per_step"] * 1e3
+            entry["config"] = workload_config(W.WORKLOADS[name])
+            per_config[name] = entry
+
+    line = {"metric": METRIC, "value": m["value"], "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "step_ms_quantiles": m["step_ms_quantiles"],
+            "dtype": w.dtype_name, "data": "synthetic", "config": workload_config(w), "run": m["run"],
+            "stage_ms": m["stage_ms"], "stage_split_ms": m["stage_split_ms"], "roofline": m["roofline"],
+            "cpu_baseline": cpu, "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": m["clocks"],
+            "routing": m["routing"], "routing_stats": routing_stats}
     if shared_ffn is not None:
         line["shared_ffn"] = shared_ffn
+    if per_config is not None:
+        line["per_config"] = per_config
     print(json.dumps(line))
     if world > 1:
         dist.barrier()

@@ -565,6 +565,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
   if ((e = make_map(&mA2, p.h, p.rows, p.F, BM * MT)) != cudaSuccess) return e;
   if ((e = make_map(&mB2, p.W2, static_cast<long long>(p.E) * p.d, p.F, BN)) != cudaSuccess) return e;
 
+  NvtxRange r1("expert_gemm1");
   GemmArgs g1{};
   g1.offsets = p.offsets;
   g1.dense_rows = p.offsets ? 0 : static_cast<int>(p.rows);
@@ -593,6 +594,7 @@ cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t bet
     if ((e = cudaEventRecordWithFlags(between_gemms, st, flags)) != cudaSuccess) return e;
   }
 
+  NvtxRange r2("expert_gemm2");
   GemmArgs g2{};
   g2.offsets = p.offsets;
   g2.dense_rows = g1.dense_rows;

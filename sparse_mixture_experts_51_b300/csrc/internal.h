@@ -8,9 +8,21 @@
 
 #include <atomic>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "moe_b300.h"
 
 namespace moe {
+
+// A named NVTX range around the host code that enqueues one stage of the
+// layer (profilers attribute the stage's kernels to it; without a profiler
+// attached the push and pop do nothing).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Kernels this library has enqueued (moe_kernel_launches).
 inline std::atomic<unsigned long long>& launch_count() {

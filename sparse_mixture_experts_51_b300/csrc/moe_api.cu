@@ -554,6 +554,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
 
   const WsLayout L = ws_layout(*shape, C);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  NvtxRange whole("moe_forward");
   // Inside a stream capture the stage events become external event-record
   // nodes, which record (and time) on every graph launch.
   unsigned int rec_flags = cudaEventRecordDefault;
@@ -579,6 +580,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   // the shared experts need no routing: their FFN runs first
   float* y_sh = nullptr;
   if (shape->d_ff_shared > 0) {
+    NvtxRange r("shared_ffn");
     y_sh = at<float>(ws, L.y_shared);
     if ((st = shared_impl(shape, x, shared, y_sh, ws, L, s)) != MOE_OK) return st;
   }
@@ -587,8 +589,12 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   moe_shape_t cshape = *shape;  // the combine's view: k ranks per token
   if (ec) {
     EcParams ep{};
-    if ((st = ec_route_impl(shape, x, W_g, b_g, W_noise, eps, logits, ws, L, s, ep)) != MOE_OK) return st;
+    {
+      NvtxRange r("router_expert_choice");
+      if ((st = ec_route_impl(shape, x, W_g, b_g, W_noise, eps, logits, ws, L, s, ep)) != MOE_OK) return st;
+    }
     if ((st = mark(1)) != MOE_OK) return st;
+    NvtxRange r("dispatch_gather");
     if (shape->T == 0) {
       if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * shape->E, s) != cudaSuccess ||
           cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (shape->E + 1), s) != cudaSuccess ||
@@ -608,10 +614,14 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     cshape.k = shape->E;
   } else {
     int32_t* backup = shape->overflow == MOE_OVERFLOW_REROUTE ? at<int32_t>(ws, L.rr_backup) : nullptr;
-    if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s,
-                         at<void>(ws, L.rt_scratch), L.rt_scratch_bytes)) != MOE_OK)
-      return st;
+    {
+      NvtxRange r("router");
+      if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s,
+                           at<void>(ws, L.rt_scratch), L.rt_scratch_bytes)) != MOE_OK)
+        return st;
+    }
     if ((st = mark(1)) != MOE_OK) return st;
+    NvtxRange r("dispatch_gather");
     if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
                             s, -1, row_of, backup)) != MOE_OK)
       return st;
@@ -635,13 +645,16 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   fp.rows = L.rows;
   fp.err = at<int>(ws, L.err);
   if (shape->dtype == MOE_BF16) {
+    // launch_ffn_bf16 names its two GEMMs (expert_gemm1, expert_gemm2) itself
     if ((st = cuda_status(launch_ffn_bf16(fp, s, stage_events ? static_cast<cudaEvent_t>(stage_events[3]) : nullptr))) != MOE_OK)
       return st;
   } else {
+    NvtxRange r("expert_ffn_f32");
     if ((st = cuda_status(launch_ffn_f32(fp, s))) != MOE_OK) return st;
     if ((st = mark(3)) != MOE_OK) return st;
   }
   if ((st = mark(4)) != MOE_OK) return st;
+  NvtxRange rc("combine");
   if ((st = combine_impl(&cshape, L.rows, y_perm, idx, gate, pos, offsets, x, y_sh, out, moe_out, at<int>(ws, L.err), s,
                         row_of)) != MOE_OK)
     return st;
