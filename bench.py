@@ -252,11 +252,11 @@ class ClockSampler:
 _ORACLE_CACHE = {}
 
 
-def cpu_oracle_run(w, budget_s: float, threads=None):
+def _oracle_timed(w, budget_s: float, rate: float):
     """Time the fp64 oracle, as it stands, on a sub-batch of the workload (the
-    same layer with its first T_s tokens as their own batch) for about
-    budget_s seconds, on all host threads or on ``threads`` BLAS threads.
-    Returns (tokens/s, sample description, threads used, seconds)."""
+    same layer with its first T_s tokens as their own batch, T_s sized from
+    the expected fp64 rate) for about budget_s seconds.
+    Returns (tokens/s, runs, T_s, seconds)."""
     from oracle import moe_oracle as O
     from sparse_mixture_experts_51_b300 import workloads as W
 
@@ -270,11 +270,9 @@ def cpu_oracle_run(w, budget_s: float, threads=None):
                 self.cache[e] = W.as_f64_numpy(self.t[e])
             return self.cache[e]
 
-    # sub-batch size from the algorithmic work per token (fp64 BLAS ~1e11 flop/s on all threads)
     per_tok = 2.0 * w.d * (3 if w.act == W.ACT_SWIGLU else 2) * (w.F * w.k + w.n_shared * w.F_shared) + 2.0 * w.d * w.E
-    rate = 1e11 if threads is None else 5e9
     T_s = int(max(16, min(w.T, budget_s * rate / per_tok / 2)))
-    key = (w.name, T_s)
+    key = (w.name, w.seed, T_s)
     if key not in _ORACLE_CACHE:
         _ORACLE_CACHE.clear()  # one workload's widened weights at a time
         inp = W.make_inputs(w.scaled(T_s))
@@ -293,28 +291,53 @@ def cpu_oracle_run(w, budget_s: float, threads=None):
         else:
             O.forward(x, Wg, w.k, w.act, W1, W2, **args)
 
-    limiter = None
-    if threads is not None:
-        from threadpoolctl import threadpool_limits
-        limiter = threadpool_limits(limits=threads)
-    try:
-        run()  # widens the expert weights to fp64 once (not timed)
-        runs, tokens, t0 = 0, 0, time.perf_counter()
-        while True:
-            run()
-            runs += 1
-            tokens += T_s
-            el = time.perf_counter() - t0
-            if el >= budget_s or runs >= 1000:
-                break
-    finally:
-        if limiter is not None:
-            limiter.unregister()
-    cores = os.cpu_count() if threads is None else threads
+    run()  # widens the expert weights to fp64 once (not timed)
+    runs, tokens, t0 = 0, 0, time.perf_counter()
+    while True:
+        run()
+        runs += 1
+        tokens += T_s
+        el = time.perf_counter() - t0
+        if el >= budget_s or runs >= 1000:
+            break
+    return tokens / el, runs, T_s, el
+
+
+def _oracle_child(name: str, seed: int, budget_s: float, threads: int) -> None:
+    """Entry point of the one-thread oracle sample (a fresh interpreter whose
+    BLAS was loaded with its thread count set in the environment)."""
+    from sparse_mixture_experts_51_b300 import workloads as W
+    w = W.WORKLOADS[name].with_(seed=seed)
+    print(json.dumps(_oracle_timed(w, budget_s, rate=5e9 * threads)))
+
+
+def cpu_oracle_run(w, budget_s: float, threads=None):
+    """The fp64 oracle on a bounded sub-batch of ``w`` for about budget_s
+    seconds: in this process on all host threads, or (``threads`` given) in
+    a child interpreter whose BLAS runs that many threads (BLAS libraries
+    read their thread count when they load).
+    Returns (tokens/s, sample description, threads used, seconds)."""
+    if threads is None:
+        v, runs, T_s, el = _oracle_timed(w, budget_s, rate=1e11)
+        cores = os.cpu_count()
+        how = "BLAS on all host threads"
+    else:
+        import subprocess
+        env = dict(os.environ)
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                    "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+            env[var] = str(threads)
+        code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+                f"bench._oracle_child({w.name!r}, {int(w.seed)}, {float(budget_s)}, {int(threads)})")
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        if r.returncode != 0:
+            raise RuntimeError(f"one-thread oracle sample failed: {r.stderr[-2000:]}")
+        v, runs, T_s, el = json.loads(r.stdout.strip().splitlines()[-1])
+        cores = threads
+        how = f"BLAS on {threads} thread(s) (a child process started with the BLAS thread variables set)"
     sample = (f"{runs} oracle forward(s) of a {T_s}-token sub-batch of {w.name} (its own capacity "
-              f"ceil({w.capacity_factor}*{T_s}*{w.k}/{w.E})), fp64 NumPy, "
-              + ("BLAS on all host threads" if threads is None else f"BLAS on {threads} thread(s)"))
-    return tokens / el, sample, cores, el
+              f"ceil({w.capacity_factor}*{T_s}*{w.k}/{w.E})), fp64 NumPy, " + how)
+    return v, sample, cores, el
 
 
 # ---------------------------------------------------------------- ranks
@@ -453,19 +476,23 @@ class DeviceLayer:
         return api.get_device_error(self.ws)
 
 
-# events of the headline timing: before the router, around expert GEMM 1 (the
-# roofline kernel) and after the combine; none inside the router -> dispatch
-# -> gather and GEMM 2 -> combine chains, whose kernels overlap their
-# neighbours' tails through programmatic dependent launch
-TIMED_SLOTS = (0, 2, 3, 5)
+# events of the headline timing: before the router and after the combine
+# only.  An event recorded between two kernels cuts their overlap
+# (programmatic dependent launch lets a kernel start while its predecessor
+# finishes, and the decode-sized layer's expert FFN start while the routing
+# runs), so the spans come from a second, shorter run with events around
+# expert GEMM 1 (the roofline kernel)
+TIMED_SLOTS = (0, 5)
+SPAN_SLOTS = (0, 2, 3, 5)
 SPANS = {"router_dispatch_gather": (0, 2), "expert_gemm1": (2, 3), "expert_gemm2_combine": (3, 5)}
+SPAN_STEPS = 50
 # the per-stage split takes every event (which cuts the overlap between stages)
 STAGE_SPANS = {"router": (0, 1), "dispatch_gather": (1, 2), "expert_gemm1": (2, 3), "expert_gemm2": (3, 4),
                "combine": (4, 5)}
 GRAPH_STEPS = 250
 
 
-def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=SPANS, sampler=None, barrier=None):
+def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=None, sampler=None, barrier=None):
     """Time ``steps`` layer forwards (moe_forward_timed; CUDA graphs of up to
     GRAPH_STEPS steps, the L2 flush before each step outside its events).
     Returns per-step device times (ms) and the per-step span times."""
@@ -494,6 +521,7 @@ def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=SPANS, sam
             torch.cuda.synchronize()
             graphs[n] = gr
 
+    spans = spans or {}
     step_ms, span_ms = [], {k: [] for k in spans}
     with (sampler if sampler is not None else contextlib.nullcontext()):
         if sampler is not None:
@@ -542,11 +570,24 @@ def roofline_of(L, work, gemm1_ms, step_ms_mean, peaks, long_run):
                 "algorithmic_flops": work["gemm1_flops"], "ms_per_launch": gemm1_ms, "traffic": traffic,
                 "layer_tflops": work["ffn_flops"] / (step_ms_mean / 1e3) / 1e12}
     ach = work["layer_bytes"] / (step_ms_mean / 1e3) / 1e9
-    return {"kernel": "whole step (expert weight stream: both expert GEMMs)", "bound": "hbm", "achieved": ach,
+    roof = {"kernel": "whole step (expert weight stream: both expert GEMMs)", "bound": "hbm", "achieved": ach,
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
             "peak_source": peaks["source"] + " copy bandwidth", "frac_of_nominal_8tbs": ach / HBM_NOMINAL_GBS,
-            "algorithmic_bytes": work["layer_bytes"], "weight_bytes": work["weight_bytes"],
-            "gemm1_gbs": work["gemm1_bytes"] / (gemm1_ms / 1e3) / 1e9, "gemm1_ms": gemm1_ms, "traffic": traffic}
+            "algorithmic_bytes": work["layer_bytes"], "weight_bytes": work["weight_bytes"], "traffic": traffic}
+    if fused_decode_ffn(w):
+        # one kernel runs both expert GEMMs (the span between stage events 2 and 3)
+        roof.update({"ffn_kernel": "ffn_decode_kernel (both expert GEMMs, fused)", "ffn_ms": gemm1_ms,
+                     "ffn_weight_gbs": work["weight_bytes"] / (gemm1_ms / 1e3) / 1e9})
+    else:
+        roof.update({"gemm1_gbs": work["gemm1_bytes"] / (gemm1_ms / 1e3) / 1e9, "gemm1_ms": gemm1_ms})
+    return roof
+
+
+def fused_decode_ffn(w) -> bool:
+    """Whether the library runs this layer's expert FFN as its fused decode
+    kernel (bf16, token choice, T <= 128 and T*k >= 4E: the rule in
+    ffn_decode.cu)."""
+    return w.dtype_name == "bf16" and w.routing == "token" and 1 <= w.T <= 128 and w.T * w.k >= 4 * w.E
 
 
 def e2e_of(L, n_steps, warmup, world=1):
@@ -767,11 +808,13 @@ def measure(L, a, flush, peaks, steps, e2e_steps, world=1, sampler_index=0, barr
     torch.cuda.synchronize()
 
     sampler = ClockSampler(sampler_index)
-    step_ms, span_ms = time_steps(L, steps, flush, eager=a.eager, sampler=sampler, barrier=barrier)
+    step_ms, _ = time_steps(L, steps, flush, eager=a.eager, sampler=sampler, barrier=barrier)
     if L.device_error() != 0:
         raise RuntimeError(f"{w.name}: device-side error during the timed region")
     total_ms = max_over_ranks(sum(step_ms), world, L.dev)
-    # the per-stage split, every stage event recorded (outside the timed region)
+    # outside the timed region: the spans around expert GEMM 1, and the
+    # per-stage split with every stage event recorded
+    _, span_ms = time_steps(L, min(steps, SPAN_STEPS), flush, eager=a.eager, slots=SPAN_SLOTS, spans=SPANS)
     _, stage = time_steps(L, min(steps, 20), flush, eager=a.eager, slots=tuple(range(6)), spans=STAGE_SPANS)
     routing, counts, dropped = routing_counts(L)
     work = layer_work(w, counts)
@@ -782,6 +825,10 @@ def measure(L, a, flush, peaks, steps, e2e_steps, world=1, sampler_index=0, barr
         "value": job_throughput(w.T, steps, world, total_ms), "ms_per_step": mean_step, "steps": steps,
         "step_ms_quantiles": step_quantiles(step_ms),
         "stage_ms": {k: statistics.mean(v) for k, v in span_ms.items()},
+        "stage_ms_note": (f"a separate run of {min(steps, SPAN_STEPS)} steps with events before the router, "
+                          "around expert GEMM 1 and after the combine (the events cut the overlap at those borders)"
+                          + ("; expert_gemm1 is the fused decode FFN (both expert GEMMs)" if fused_decode_ffn(w)
+                             else "")),
         "stage_split_ms": {k: statistics.mean(v) for k, v in stage.items()},
         "stage_split_note": "every stage event recorded: no programmatic-launch overlap across the stage borders",
         "roofline": roofline_of(L, work, gemm1_ms, mean_step, peaks, long_run),

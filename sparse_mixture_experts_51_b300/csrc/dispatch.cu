@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(NT) dispatch_kernel(DispatchParams p) {
   const int E = p.E;
   const long long total = static_cast<long long>(p.T) * p.k;
 
+  if (p.early_trigger) pdl_trigger();
   pdl_wait();  // the top-k table is the predecessor's output
   if (tid == 0) s_ticket = atomicAdd(&p.ctrl[0], 1);
   for (int i = tid; i < ITEMS * NWARP * E; i += NT) s_hist[i] = 0;
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(SNT, 1) dispatch_single_kernel(DispatchParams 
   constexpr int S = ITEMS * SNW;  // (step, warp) entries per expert
 
   for (int i = tid; i < S * E; i += SNT) s_hist[i] = 0;
+  if (p.early_trigger) pdl_trigger();
   pdl_wait();  // the top-k table is the predecessor's output
   // per item: expert + 1 in bits 0-7 (0: none), rank inside the warp step in bits 8-12
   int my_er[ITEMS];

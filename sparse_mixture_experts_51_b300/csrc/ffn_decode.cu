@@ -1,0 +1,561 @@
+// Expert FFN of a decode-sized batch (T <= 128 tokens) as one persistent
+// tcgen05 kernel whose first phase does not wait for the routing.
+//
+// With T <= 128 every expert's rows fit one 128-row M tile, so computing an
+// expert over ALL T tokens costs the tensor cores exactly what computing it
+// over its kept rows costs (the same single M tile), and each output row
+// depends only on its own input row: the rows of the kept (token, expert)
+// pairs come out bit for bit as the grouped GEMMs give them.  The layer is
+// then a stream of expert weights (SwiGLU: 3 d F bytes per expert, GELU:
+// 2 d F), and the stream can start before the router has finished:
+//
+//   phase 1  h_all[e*128 + t] = act(x[t] W1[e]^T (, x[t] W3[e]^T)) for every
+//            expert e and token t < T (rows t >= T are zero-filled by TMA and
+//            never read back); one tile = expert e x 128 (SwiGLU) or 256
+//            (GELU) columns of h, A = the token matrix itself
+//   phase 2  y_perm[offsets[e] + pos[t,r]] = h_all[e*128 + t] W2[e]^T + b2[e]
+//            for every kept assignment (t, r) of expert e: the epilogue
+//            scatters each row to its grouped row (the combine's layout),
+//            other rows are not stored; one tile = expert e x 256 columns
+//
+// (the expert FFN of "Mixture-of-Experts Sparse Model Scaling", Core
+// Concepts; a dropped assignment skips its expert as in "LLM part 09", s3:
+// its row is computed but never stored or combined).
+//
+// Tiles are claimed one at a time from a ticket in the workspace: every
+// phase-1 tile before every phase-2 tile, experts in order.  A phase-2 tile
+// of expert e waits until all phase-1 tiles of e have stored their rows (a
+// per-expert count of finished epilogue warps).  Every tile a CTA waits on
+// was claimed earlier by a CTA that is running and does not wait on
+// anything later, so the waits always end.  The routing tables (idx, pos,
+// offsets) are read only after griddepcontrol.wait; a phase-2 tile of an
+// expert without kept rows is skipped.  The last CTA to finish clears the
+// ticket and counts for the next call.
+//
+// Roles per CTA (384 threads): warp 0 claims tiles and issues TMA loads
+// (4-stage ring of 48 KB: A 128x64, B 256x64, 128-byte swizzle); warp 1
+// issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators;
+// warp 2 owns TMEM; warps 4-11 drain the accumulator (two per TMEM lane
+// quarter, half of the 32-column chunks each) with whole-sector stores.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGES = 4;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NACC = 2;
+constexpr int ACC_COLS = 256;
+constexpr int TMEM_COLS = NACC * ACC_COLS;
+constexpr int NTHREADS = 384;
+constexpr int EPI_WARPS = 8;
+constexpr int QN = 4;  // tile-queue slots (claimed tiles handed from the producer to the other roles)
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers, queue*/;
+
+struct DecodeArgs {
+  int T, d, F, E, k;
+  int swiglu;
+  int n1, n2;    // N tiles per expert: phase 1 (128 h columns SwiGLU, 256 GELU), phase 2 (256 y columns)
+  int kb1, kb2;  // 64-wide k-blocks: d / 64, F / 64
+  const float* b1;  // [E, F] or null (GELU)
+  const float* b2;  // [E, d] or null
+  __nv_bfloat16* h;  // [E*128, F] phase-1 output
+  const int32_t* idx;
+  const int32_t* pos;
+  const int32_t* offsets;
+  float* y;        // [rows, d]
+  long long rows;  // allocated rows of y
+  int* ctrl;       // [0] ticket, [1] finished CTAs, [2, 2+E) finished phase-1 epilogue warps per expert
+  int* err;
+};
+
+__device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
+// silu(a) = a (1 + tanh(a/2)) / 2 with the hardware tanh approximation, as
+// in the grouped GEMM (the same formula, so the rows agree bit for bit)
+__device__ __forceinline__ float tanh_approx(float v) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float silu_f(float a) {
+  const float h = 0.5f * a;
+  return fmaf(h, tanh_approx(h), h);
+}
+
+__device__ __forceinline__ void st_global_32b(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w),
+               "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// orders this thread's generic-proxy accesses before its later async-proxy
+// (TMA) accesses of global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    ffn_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
+                      const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmH,
+                      const __grid_constant__ CUtensorMap tmW2, DecodeArgs g) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* tiles = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + STAGES * STAGE_BYTES);
+  uint64_t* full = bars;                 // [STAGES]
+  uint64_t* empty = full + STAGES;       // [STAGES]
+  uint64_t* tfull = empty + STAGES;      // [NACC]
+  uint64_t* tempty = tfull + NACC;       // [NACC]
+  uint64_t* qfull = tempty + NACC;       // [QN]
+  uint64_t* qempty = qfull + QN;         // [QN]
+  uint64_t* drain = qempty + QN;         // [1]
+  int* s_tile = reinterpret_cast<int*>(drain + 1);  // [QN]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_tile + QN);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int E = g.E;
+  const int total1 = E * g.n1;
+  const int total = total1 + E * g.n2;
+  int* ticket = g.ctrl;
+  int* finished = g.ctrl + 1;
+  int* done1 = g.ctrl + 2;
+  const int done_target = EPI_WARPS * g.n1;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < NACC; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), EPI_WARPS);
+    }
+    for (int q = 0; q < QN; ++q) {
+      mbar_init(smem_u32(&qfull[q]), 1);
+      mbar_init(smem_u32(&qempty[q]), 1 + EPI_WARPS);  // the MMA thread and every epilogue warp
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW1);
+    if (g.swiglu) tma_prefetch_desc(&tmW3);
+    tma_prefetch_desc(&tmH);
+    tma_prefetch_desc(&tmW2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // No griddepcontrol.wait here: phase 1 reads only the tokens and the
+  // weights, which were complete before the router (the first kernel of the
+  // chain that launched this one) passed its own wait.
+
+  if (warp == 0) {
+    // ================= tile claims + TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, last_phase = 0;
+      int q = 0;
+      uint32_t qphase = 0;
+      bool routed = false, ok = true;
+      while (true) {
+        int id = -1;
+        if (ok) {
+          // claim the next tile with work (phase-2 tiles of experts without kept rows are skipped)
+          while (true) {
+            id = atomicAdd(ticket, 1);
+            if (id >= total) { id = -1; break; }
+            if (id < total1) break;
+            if (!routed) {
+              pdl_wait();  // the routing tables are complete from here on
+              routed = true;
+            }
+            const int e = (id - total1) / g.n2;
+            if (__ldcg(g.offsets + e + 1) > __ldcg(g.offsets + e)) break;
+          }
+        }
+        // hand it to the MMA thread and the epilogue warps (-1: no more tiles)
+        if (!mbar_wait_bounded(smem_u32(&qempty[q]), qphase ^ 1u, g.err, abort_flag)) id = -1;
+        s_tile[q] = id;
+        mbar_arrive(smem_u32(&qfull[q]));
+        if (++q == QN) { q = 0; qphase ^= 1u; }
+        if (id < 0) break;
+
+        const bool p1 = id < total1;
+        const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
+        const int nb = p1 ? id - e * g.n1 : (id - total1) - e * g.n2;
+        const int KB = p1 ? g.kb1 : g.kb2;
+        // phase 2: the B panel needs nothing; A (expert e's rows of h) needs
+        // every phase-1 tile of e stored.  Issue the first stages' B loads,
+        // then wait, then their A loads.
+        bool h_ready = p1 || ld_acquire(done1 + e) >= done_target;
+        if (!p1 && h_ready) fence_proxy_async_global();  // the TMA loads of h follow the acquire
+        int pend_stage[STAGES];
+        int npend = 0;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, g.err, abort_flag)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint32_t sb = sa + A_BYTES;
+          if (p1) {
+            tma_load_2d(sa, &tmX, fb, kb * BK, 0);
+            if (g.swiglu) {
+              tma_load_2d(sb, &tmW1, fb, kb * BK, e * g.F + nb * 128);
+              tma_load_2d(sb + B_BYTES / 2, &tmW3, fb, kb * BK, e * g.F + nb * 128);
+            } else {
+              tma_load_2d(sb, &tmW1, fb, kb * BK, e * g.F + nb * BN);
+            }
+          } else {
+            tma_load_2d(sb, &tmW2, fb, kb * BK, e * g.d + nb * BN);
+            if (h_ready) {
+              tma_load_2d(sa, &tmH, fb, kb * BK, e * BM);
+            } else {
+              pend_stage[npend++] = stage;
+              if (npend == STAGES || kb == KB - 1) {
+                // bounded wait for the phase-1 rows of expert e
+                const unsigned long long t0 = globaltimer_ns();
+                while (ld_acquire(done1 + e) < done_target) {
+                  if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                    record_error(g.err, MOE_ERR_DEVICE_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                  }
+                }
+                // the TMA loads of h below are ordered after the acquire (the
+                // pending stages still get their A copies so that every
+                // expected transaction arrives)
+                fence_proxy_async_global();
+                for (int i = 0; i < npend; ++i) {
+                  const int s2 = pend_stage[i];
+                  const int kb2 = kb - (npend - 1 - i);
+                  tma_load_2d(smem_u32(tiles + s2 * STAGE_BYTES), &tmH, smem_u32(&full[s2]), kb2 * BK, e * BM);
+                }
+                npend = 0;
+                h_ready = true;
+              }
+            }
+          }
+          issued |= 1u << stage;
+          last_phase = (last_phase & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          if (!ok) break;
+        }
+      }
+      // no copy into this CTA's shared memory is still in flight
+      for (int s = 0; s < STAGES; ++s)
+        if (issued >> s & 1u) mbar_wait_bounded(smem_u32(&full[s]), (last_phase >> s) & 1u, g.err, nullptr);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t aphase = 0;
+      int q = 0;
+      uint32_t qphase = 0;
+      bool any = false;
+      while (true) {
+        if (!mbar_wait_bounded(smem_u32(&qfull[q]), qphase, g.err, abort_flag)) break;
+        const int id = s_tile[q];
+        mbar_arrive(smem_u32(&qempty[q]));
+        if (++q == QN) { q = 0; qphase ^= 1u; }
+        if (id < 0) break;
+        const int KB = id < total1 ? g.kb1 : g.kb2;
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aphase ^ 1u, g.err, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem_base + static_cast<uint32_t>(acc * ACC_COLS);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, g.err, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tiles + stage * STAGE_BYTES);
+          const uint64_t da = smem_desc_sw128(sa);
+          const uint64_t db = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(dt, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), IDESC,
+                      (kb | kk) != 0 ? 1u : 0u);
+          umma_commit(smem_u32(&empty[stage]));
+          any = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[acc]));
+        if (++acc == NACC) { acc = 0; aphase ^= 1u; }
+      }
+      if (any) {
+        umma_commit(smem_u32(drain));
+        mbar_wait_bounded(smem_u32(drain), 0, g.err, nullptr);
+      }
+    }
+  } else if (warp >= 4) {
+    // ================= epilogue =================
+    const int qd = warp & 3;             // TMEM lane quarter
+    const int half = (warp - 4) >> 2;    // which half of the tile's 32-column chunks
+    const int t = qd * 32 + lane;        // token (row of the tile)
+    int acc = 0;
+    uint32_t aphase = 0;
+    int q = 0;
+    uint32_t qphase = 0;
+    bool routed = false;
+    while (true) {
+      if (!mbar_wait_bounded(smem_u32(&qfull[q]), qphase, g.err, abort_flag)) break;
+      const int id = s_tile[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&qempty[q]));
+      if (++q == QN) { q = 0; qphase ^= 1u; }
+      if (id < 0) break;
+      const bool p1 = id < total1;
+      const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
+      const int nb = p1 ? id - e * g.n1 : (id - total1) - e * g.n2;
+      // phase 2: the grouped row this token's assignment to e was given (-1: none or dropped)
+      long long dest = -1;
+      if (!p1) {
+        if (!routed) {
+          pdl_wait();
+          routed = true;
+        }
+        if (t < g.T) {
+          for (int r = 0; r < g.k; ++r) {
+            const long long a = static_cast<long long>(t) * g.k + r;
+            if (__ldcg(g.idx + a) == e) {
+              const int ps = __ldcg(g.pos + a);
+              if (ps >= 0) dest = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
+            }
+          }
+          if (dest >= g.rows) {
+            record_error(g.err, MOE_ERR_BOUNDS);
+            dest = -1;
+          }
+        }
+      }
+      if (!mbar_wait_bounded(smem_u32(&tfull[acc]), aphase, g.err, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + static_cast<uint32_t>(acc * ACC_COLS);
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      };
+      if (p1 && g.swiglu) {
+        // 4 chunks of 32 h columns (gate at TMEM column c*32, up at 128 + c*32); two per warp
+        __nv_bfloat16* hrow = g.h + (static_cast<long long>(e) * BM + t) * g.F;
+#pragma unroll 1
+        for (int c = half * 2; c < half * 2 + 2; ++c) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32_issue(tbase + c * 32, gr);
+          tmem_ld32_issue(tbase + 128 + c * 32, ur);
+          tmem_wait_ld(gr, ur);
+          if (c == half * 2 + 1) release();
+          const int col = nb * 128 + c * 32;
+          if (col < g.F) {
+            uint4 pk[4];
+            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              h2[i] = __floats2bfloat162_rn(silu_f(__uint_as_float(gr[2 * i])) * __uint_as_float(ur[2 * i]),
+                                            silu_f(__uint_as_float(gr[2 * i + 1])) * __uint_as_float(ur[2 * i + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(hrow + col);
+            st_global_32b(dst, pk[0], pk[1]);
+            st_global_32b(dst + 2, pk[2], pk[3]);
+          }
+        }
+      } else {
+        // 8 chunks of 32 columns, four per warp, two in flight per wait
+#pragma unroll 1
+        for (int c = half * 4; c < half * 4 + 4; c += 2) {
+          uint32_t r0[32], r1[32];
+          tmem_ld32_issue(tbase + c * 32, r0);
+          tmem_ld32_issue(tbase + (c + 1) * 32, r1);
+          tmem_wait_ld(r0, r1);
+          if (c + 2 >= half * 4 + 4) release();
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t* v = j == 0 ? r0 : r1;
+            const int col = nb * BN + (c + j) * 32;
+            if (p1) {
+              // GELU: h = gelu(a + b1)
+              if (col < g.F) {
+                const float* bias = g.b1 ? g.b1 + static_cast<long long>(e) * g.F + col : nullptr;
+                uint4 pk[4];
+                __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  float a0 = __uint_as_float(v[2 * i]), a1 = __uint_as_float(v[2 * i + 1]);
+                  if (bias) { a0 += bias[2 * i]; a1 += bias[2 * i + 1]; }
+                  h2[i] = __floats2bfloat162_rn(gelu_f(a0), gelu_f(a1));
+                }
+                uint4* dst = reinterpret_cast<uint4*>(g.h + (static_cast<long long>(e) * BM + t) * g.F + col);
+                st_global_32b(dst, pk[0], pk[1]);
+                st_global_32b(dst + 2, pk[2], pk[3]);
+              }
+            } else if (dest >= 0 && col < g.d) {
+              // down projection: y = a + b2, scattered to the assignment's grouped row
+              const float* bias = g.b2 ? g.b2 + static_cast<long long>(e) * g.d + col : nullptr;
+              uint4 o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                       __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+                if (bias) { f.x += bias[4 * i]; f.y += bias[4 * i + 1]; f.z += bias[4 * i + 2]; f.w += bias[4 * i + 3]; }
+                o[i] = make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+              }
+              uint4* dst = reinterpret_cast<uint4*>(g.y + dest * g.d + col);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_global_32b(dst + 2 * i, o[2 * i], o[2 * i + 1]);
+            }
+          }
+        }
+      }
+      if (p1) {
+        // this warp's rows of the tile are stored: count it for expert e (the
+        // phase-2 tiles of e read these rows through TMA after the count is complete)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(done1 + e, 1);
+      }
+      if (++acc == NACC) { acc = 0; aphase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  // the routing tables are complete before this grid is (the combine after
+  // it relies on that), whatever tiles this CTA took
+  pdl_wait();
+  __syncthreads();
+  if (tid == 0) {
+    // the last CTA to get here clears the ticket and counts for the next call
+    __threadfence();
+    if (atomicAdd(finished, 1) == static_cast<int>(gridDim.x) - 1) {
+      *ticket = 0;
+      for (int e = 0; e < E; ++e) done1[e] = 0;
+      __threadfence();
+      *finished = 0;
+      __threadfence();
+    }
+    pdl_trigger();
+  }
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+      g_encode_err = e != cudaSuccess ? e : cudaErrorSymbolNotFound;
+      return;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode_err;
+}
+
+// bf16 [rows, K] (K contiguous) read in boxes of box_rows x 64, 128-byte swizzle
+cudaError_t make_map(CUtensorMap* m, const void* base, long long rows, int K, int box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+bool ffn_decode_applies(const moe_shape_t& s) {
+  // every expert's rows fit one 128-row tile, and enough assignments that
+  // (nearly) every expert is expected to be active: the dense phase 1 then
+  // streams no weights the grouped GEMMs would not
+  return s.dtype == MOE_BF16 && s.routing == MOE_ROUTE_TOKEN_CHOICE && s.T >= 1 && s.T <= BM &&
+         s.T * static_cast<long long>(s.k) >= 4LL * s.E && s.d % 64 == 0 && s.d_ff % 64 == 0;
+}
+
+size_t ffn_decode_h_bytes(const moe_shape_t& s) { return static_cast<size_t>(s.E) * BM * s.d_ff * 2; }
+size_t ffn_decode_ctrl_bytes(const moe_shape_t& s) { return sizeof(int) * (2 + static_cast<size_t>(s.E)); }
+
+cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st) {
+  cudaError_t e = get_encoder();
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const bool swiglu = p.act == MOE_ACT_SWIGLU;
+  CUtensorMap mX, mW1, mW3, mH, mW2;
+  if ((e = make_map(&mX, p.x, p.T, p.d, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mW1, p.W1, static_cast<long long>(p.E) * p.F, p.d, swiglu ? BN / 2 : BN)) != cudaSuccess) return e;
+  if (swiglu) {
+    if ((e = make_map(&mW3, p.W3, static_cast<long long>(p.E) * p.F, p.d, BN / 2)) != cudaSuccess) return e;
+  } else {
+    mW3 = mW1;
+  }
+  if ((e = make_map(&mH, p.h, static_cast<long long>(p.E) * BM, p.F, BM)) != cudaSuccess) return e;
+  if ((e = make_map(&mW2, p.W2, static_cast<long long>(p.E) * p.d, p.F, BN)) != cudaSuccess) return e;
+  DecodeArgs g{};
+  g.T = p.T;
+  g.d = p.d;
+  g.F = p.F;
+  g.E = p.E;
+  g.k = p.k;
+  g.swiglu = swiglu ? 1 : 0;
+  g.n1 = swiglu ? (p.F + 127) / 128 : (p.F + BN - 1) / BN;
+  g.n2 = (p.d + BN - 1) / BN;
+  g.kb1 = p.d / BK;
+  g.kb2 = p.F / BK;
+  g.b1 = p.b1;
+  g.b2 = p.b2;
+  g.h = static_cast<__nv_bfloat16*>(p.h);
+  g.idx = p.idx;
+  g.pos = p.pos;
+  g.offsets = p.offsets;
+  g.y = p.y_perm;
+  g.rows = p.rows;
+  g.ctrl = p.ctrl;
+  g.err = p.err;
+  if ((e = cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
+      cudaSuccess)
+    return e;
+  const long long tiles = static_cast<long long>(p.E) * (g.n1 + g.n2);
+  const int grid = static_cast<int>(std::min<long long>(sms, tiles));
+  NvtxRange r("expert_ffn_decode");
+  return launch_pdl(ffn_decode_kernel, dim3(grid), dim3(NTHREADS), static_cast<size_t>(SMEM_BYTES), st, 1, mX, mW1,
+                    mW3, mH, mW2, g);
+}
+
+}  // namespace moe

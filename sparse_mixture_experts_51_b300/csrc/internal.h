@@ -99,6 +99,9 @@ struct WsLayout {
   size_t x_perm;             // [R,d] dtype
   size_t h;                  // [R,F] dtype
   size_t y_perm;             // [R,d] fp32
+  size_t dec_h;              // decode-sized batches: [E*128, d_ff] bf16 hidden rows of every (expert, token)
+  size_t dec_ctrl;           // and the fused FFN's tile ticket and per-expert counts
+  bool dec;                  // the fused decode FFN applies (ffn_decode_applies)
   size_t total;
   int nblk_dispatch;
   int64_t rows;              // R = min(T*k, E*C)
@@ -140,6 +143,7 @@ struct RouterParams {
   int* err;
   void* scratch;    // workspace room for the tensor-core filter path (null: CUDA cores only)
   size_t scratch_bytes;
+  int early_trigger;  // 1: let the next kernel launch right after this one's own wait on its predecessor
 };
 cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st);
 // the tensor-core filter router (router_tc.cu) for wide logit tables of bf16 layers
@@ -158,6 +162,7 @@ struct DispatchParams {
   long long* dropped;
   int* ctrl;       // ticket, status[nblk], done counter
   int clear_ctrl;  // 1: zero ctrl before the kernel; 0: it is zero already (the last block resets it)
+  int early_trigger;  // 1: let the next kernel launch at once (it waits for this one before reading its outputs)
   int* agg;        // [nblk][E]
   int* incl;       // [nblk][E]
   int nblk;
@@ -212,6 +217,31 @@ struct FfnParams {
   long long rows;  // allocated rows of x_perm / h / y_perm
   int* err;
 };
+// The expert FFN of a decode-sized batch (ffn_decode.cu): one persistent
+// kernel, phase 1 dense over all T <= 128 tokens (no routing needed), phase 2
+// scattered to the kept assignments' grouped rows of y_perm.
+struct DecodeFfnParams {
+  const void* x;  // [T, d] bf16 tokens
+  int T, d, F, E, k, act;
+  const void* W1;
+  const void* W3;
+  const void* W2;
+  const float* b1;
+  const float* b2;
+  void* h;                 // [E*128, F] bf16 workspace
+  const int32_t* idx;      // [T,k] routing tables (read after the routing kernels complete)
+  const int32_t* pos;
+  const int32_t* offsets;
+  float* y_perm;           // [rows, d]
+  long long rows;
+  int* ctrl;               // 2 + E ints, zero at first use (self-resetting)
+  int* err;
+};
+bool ffn_decode_applies(const moe_shape_t& s);
+size_t ffn_decode_h_bytes(const moe_shape_t& s);
+size_t ffn_decode_ctrl_bytes(const moe_shape_t& s);
+cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st);
+
 // between_gemms (optional) is recorded on `st` after the first GEMM is enqueued
 cudaError_t launch_ffn_bf16(const FfnParams& p, cudaStream_t st, cudaEvent_t between_gemms = nullptr);
 cudaError_t launch_ffn_f32(const FfnParams& p, cudaStream_t st);

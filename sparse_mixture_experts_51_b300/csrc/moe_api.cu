@@ -71,6 +71,9 @@ WsLayout ws_layout(const moe_shape_t& s, int32_t C) {
   L.x_perm = take(b * static_cast<size_t>(L.rows) * s.d);
   L.h = take(b * static_cast<size_t>(L.rows) * s.d_ff);
   L.y_perm = take(sizeof(float) * static_cast<size_t>(L.rows) * s.d);
+  L.dec = ffn_decode_applies(s);
+  L.dec_h = take(L.dec ? ffn_decode_h_bytes(s) : 0);
+  L.dec_ctrl = take(L.dec ? ffn_decode_ctrl_bytes(s) : 0);
   L.total = o;
   return L;
 }
@@ -173,7 +176,7 @@ moe_status_t moe_route(const moe_shape_t* shape, const void* x, const float* W_g
 static moe_status_t route_impl(const moe_shape_t* shape, const void* x, const float* W_g, const float* b_g,
                                const float* W_noise, const float* eps, int32_t* idx, float* w, float* logits,
                                int64_t* stats, int32_t* backup, int* err, cudaStream_t st, void* scratch = nullptr,
-                               size_t scratch_bytes = 0) {
+                               size_t scratch_bytes = 0, bool early_trigger = false) {
   if (shape->T == 0) return MOE_OK;
   RouterParams p{};
   p.x = x;
@@ -194,6 +197,7 @@ static moe_status_t route_impl(const moe_shape_t* shape, const void* x, const fl
   p.err = err;
   p.scratch = scratch;
   p.scratch_bytes = scratch_bytes;
+  p.early_trigger = early_trigger ? 1 : 0;
   return cuda_status(launch_router(p, shape->dtype, st));
 }
 
@@ -259,7 +263,8 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, int32_t* 
                                   int32_t* pos, int32_t* counts, int32_t* offsets, int64_t* dropped,
                                   void* x_perm, int32_t* row_token, void* ws, const WsLayout& L,
                                   cudaStream_t st, int stall_block = -1, int32_t* row_of = nullptr,
-                                  const int32_t* backup = nullptr) {
+                                  const int32_t* backup = nullptr, bool early_trigger = false,
+                                  bool gather = true) {
   const bool rr = backup != nullptr;
   DispatchParams dp{};
   dp.idx = idx;
@@ -277,6 +282,7 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, int32_t* 
   dp.incl = at<int>(ws, L.disp_incl);
   dp.nblk = L.nblk_dispatch;
   dp.stall_block = stall_block;
+  dp.early_trigger = early_trigger ? 1 : 0;
   dp.err = at<int>(ws, L.err);
   if (rr) {
     // first pass into scratch counts / drop count; the second pass writes the real ones
@@ -306,6 +312,7 @@ static moe_status_t dispatch_impl(const moe_shape_t* shape, int32_t C, int32_t* 
     if (launch_dispatch(d2, st) != cudaSuccess) return MOE_ERR_CUDA;
     if (launch_reroute_merge(rp, st) != cudaSuccess) return MOE_ERR_CUDA;
   }
+  if (!gather) return MOE_OK;
   GatherParams gp{};
   gp.x = x;
   gp.idx = idx;
@@ -614,16 +621,19 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     cshape.k = shape->E;
   } else {
     int32_t* backup = shape->overflow == MOE_OVERFLOW_REROUTE ? at<int32_t>(ws, L.rr_backup) : nullptr;
+    // decode-sized batches: the router and the dispatch let the fused expert
+    // FFN launch at once (its first phase needs no routing), and there is no
+    // gather (the FFN reads the tokens themselves)
     {
       NvtxRange r("router");
       if ((st = route_impl(shape, x, W_g, b_g, W_noise, eps, idx, w, logits, stats, backup, nullptr, s,
-                           at<void>(ws, L.rt_scratch), L.rt_scratch_bytes)) != MOE_OK)
+                           at<void>(ws, L.rt_scratch), L.rt_scratch_bytes, L.dec)) != MOE_OK)
         return st;
     }
     if ((st = mark(1)) != MOE_OK) return st;
     NvtxRange r("dispatch_gather");
     if ((st = dispatch_impl(shape, C, idx, x, pos, counts, offsets, dropped, at<void>(ws, L.x_perm), nullptr, ws, L,
-                            s, -1, row_of, backup)) != MOE_OK)
+                            s, -1, row_of, backup, L.dec, !L.dec)) != MOE_OK)
       return st;
   }
   if ((st = mark(2)) != MOE_OK) return st;
@@ -644,7 +654,33 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   fp.act = shape->act;
   fp.rows = L.rows;
   fp.err = at<int>(ws, L.err);
-  if (shape->dtype == MOE_BF16) {
+  if (L.dec && !ec) {
+    // one kernel for both expert GEMMs (stage event 3 follows both)
+    DecodeFfnParams dp{};
+    dp.x = x;
+    dp.T = static_cast<int>(shape->T);
+    dp.d = shape->d;
+    dp.F = shape->d_ff;
+    dp.E = shape->E;
+    dp.k = shape->k;
+    dp.act = shape->act;
+    dp.W1 = W1;
+    dp.W3 = W3;
+    dp.W2 = W2;
+    dp.b1 = b1;
+    dp.b2 = b2;
+    dp.h = at<void>(ws, L.dec_h);
+    dp.idx = idx;
+    dp.pos = pos;
+    dp.offsets = offsets;
+    dp.y_perm = y_perm;
+    dp.rows = L.rows;
+    dp.ctrl = at<int>(ws, L.dec_ctrl);
+    dp.err = at<int>(ws, L.err);
+    if ((st = cuda_status(launch_ffn_decode(dp, s))) != MOE_OK) return st;
+    if ((st = mark(3)) != MOE_OK) return st;
+    row_of = nullptr;  // no gather wrote it: the combine finds the rows from idx, pos and offsets
+  } else if (shape->dtype == MOE_BF16) {
     // launch_ffn_bf16 names its two GEMMs (expert_gemm1, expert_gemm2) itself
     if ((st = cuda_status(launch_ffn_bf16(fp, s, stage_events ? static_cast<cudaEvent_t>(stage_events[3]) : nullptr))) != MOE_OK)
       return st;

@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(WT, 1) router_warp_kernel(RouterParams p, Warp
   const TX* x = static_cast<const TX*>(p.x);
 
   pdl_wait();  // tokens (and weights) may be the predecessor's output
+  if (p.early_trigger) pdl_trigger();
   // ---- stage the router weights, transposed, with 4-byte asynchronous
   // copies (all in flight at once); zero rows and tail padding
   for (int i = tid; i < d * NC; i += WT) {

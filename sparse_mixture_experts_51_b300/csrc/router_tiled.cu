@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(RT, 2) router_tiled_kernel(RouterParams p, Til
   const int nloc = max(0, min(q.nch, ch0 + q.nch_per) - ch0);
 
   pdl_wait();  // tokens (and weights) may be the predecessor's output
+  if (p.early_trigger) pdl_trigger();
   float sq[NV];
   float wsq = 0.f;  // sum of W^2 of column (tid mod NCP) over this CTA's rows
 #pragma unroll

@@ -217,7 +217,10 @@ def test_expert_choice_argument_errors(lib):
     assert _ws(lib, _shape(routing=7), 40)[0] == INVALID
     assert _ws(lib, _shape(routing=1, T=1 << 27, E=32, k=1), 40)[0] == UNSUPPORTED  # T*E >= 2^31
     st, n = _ws(lib, ec, 40)
-    assert st == OK and n > _ws(lib, tc, 40)[1]
+    assert st == OK
+    # expert choice keeps [T,E] tables the token-choice layer does not (a batch above 128 tokens,
+    # where the token-choice layer has no fused decode FFN rows either)
+    assert _ws(lib, _shape(T=300, routing=1), 40)[1] > _ws(lib, _shape(T=300), 40)[1]
     # the expert-choice route needs an expert-choice shape, its outputs and a workspace
     assert lib.moe_route_expert_choice(ctypes.byref(tc), 40, f, f, None, None, None, f, f, None, None, f, n,
                                        None) == INVALID
@@ -226,7 +229,7 @@ def test_expert_choice_argument_errors(lib):
     assert lib.moe_route_expert_choice(ctypes.byref(ec), 40, f, f, None, f, None, f, f, None, None, f, n,
                                        None) == INVALID  # W_noise without eps
     assert lib.moe_route_expert_choice(ctypes.byref(ec), 40, f, f, None, None, None, f, f, None, None, f,
-                                       _ws(lib, tc, 40)[1], None) == WORKSPACE
+                                       n - 256, None) == WORKSPACE
     # token-choice steps refuse an expert-choice shape
     assert lib.moe_dispatch(ctypes.byref(ec), 40, f, f, f, f, f, f, f, None, f, n, None) == INVALID
     assert lib.moe_combine(ctypes.byref(ec), 40, f, f, f, f, f, None, None, f, None, None) == INVALID
@@ -249,3 +252,18 @@ def test_overflow_and_gate_option_errors(lib):
     # re-routing runs only inside moe_forward
     assert lib.moe_dispatch(ctypes.byref(rr), 40, f, f, f, f, f, f, f, None, f, n, None) == INVALID
     assert lib.moe_dispatch_noalloc(ctypes.byref(rr), 40, f, f, f, f, f, f, f, None, None, None) == INVALID
+
+
+@no_gpu
+def test_decode_sized_workspace_holds_the_fused_ffn_rows(lib):
+    """A bf16 token-choice batch of at most 128 tokens with T*k >= 4E runs its
+    expert FFN densely over every (expert, token): its workspace holds E*128
+    hidden rows of d_ff bf16 values more than the grouped layout needs."""
+    small = _shape(T=128, E=4, k=2, d_ff=128)      # 256 assignments >= 16: fused
+    sparse = _shape(T=128, E=64, k=1, d_ff=128)    # 128 assignments < 256: grouped
+    grouped = _shape(T=129, E=4, k=2, d_ff=128)    # above one 128-row tile: grouped
+    f32 = _shape(T=128, E=4, k=2, d_ff=128, dtype=0)
+    n_small = _ws(lib, small, 64)[1]
+    assert n_small - _ws(lib, f32, 64)[1] >= 4 * 128 * 128 * 2 - 2 * (128 * 64 * 2 + 128 * 128 * 2)
+    assert n_small > _ws(lib, grouped, 64)[1] - 16 * 1024
+    assert _ws(lib, sparse, 64)[1] < 64 * 128 * 128 * 2
