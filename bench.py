@@ -647,7 +647,10 @@ def e2e_of(L, n_steps, warmup, world=1):
         return t0.elapsed_time(t1)
 
     run(max(2, warmup))
+    # at least ~100 ms of steps: each timed run also carries a fixed host-side start-up cost
     n = max(2, n_steps)
+    probe_ms = run(4) / 4
+    n = int(min(5000, max(n, math.ceil(100.0 / max(probe_ms, 1e-3)))))
     ms = max_over_ranks(run(n), world, dev)
     # the layer run through the public call gives the device-timed output, bit for bit
     if not torch.equal(out_host[(n - 1) % 2], L.out.cpu()):

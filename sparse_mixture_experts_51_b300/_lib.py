@@ -65,6 +65,7 @@ SIGNATURES = {
     "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_testing_dispatch_stalled": (ctypes.c_int, [_SHAPE, ctypes.c_int32] + [_P] * 7
                                      + [ctypes.c_int32, _P, ctypes.c_size_t, _P]),
+    "moe_testing_router_filter": (ctypes.c_int, [_SHAPE] + [_P] * 5 + [ctypes.c_size_t, _P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 

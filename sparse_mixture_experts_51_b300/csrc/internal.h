@@ -150,6 +150,8 @@ cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st);
 bool router_tc_applies(const RouterParams& p, int dtype);
 size_t router_tc_scratch_bytes(long long T, int d, int E);
 cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t st);
+// its weight split and filter GEMM alone: the approximate logits [T, nc] (a test hook)
+cudaError_t launch_router_tc_filter(const RouterParams& p, void* scratch, float* approx, cudaStream_t st);
 // the cluster-tiled router kernel (router_tiled.cu), for wide logit tables
 cudaError_t launch_router_tiled(const RouterParams& p, int dtype, cudaStream_t st, int sms);
 

@@ -747,6 +747,29 @@ moe_status_t moe_routing_stats(const moe_shape_t* shape, const float* logits, co
   return cuda_status(launch_routing_stats(p, static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_testing_router_filter(const moe_shape_t* shape, const void* x, const float* W_g,
+                                       const float* W_noise, float* approx, void* ws, size_t ws_bytes, void* stream) {
+  moe_status_t st = check_shape(shape);
+  if (st != MOE_OK) return st;
+  if (shape->routing != MOE_ROUTE_TOKEN_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (x == nullptr || W_g == nullptr || approx == nullptr) return MOE_ERR_INVALID_ARG;
+  const int nc = W_noise ? 2 * shape->E : shape->E;
+  if (shape->dtype != MOE_BF16 || nc % 32 != 0 || nc > 256 || shape->T < 1) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(approx)) return MOE_ERR_UNSUPPORTED;
+  if ((st = check_ws(shape, 0, ws, ws_bytes)) != MOE_OK) return st;
+  const WsLayout L = ws_layout(*shape, 0);
+  RouterParams p{};
+  p.x = x;
+  p.W_g = W_g;
+  p.W_n = W_noise;
+  p.T = static_cast<int>(shape->T);
+  p.d = shape->d;
+  p.E = shape->E;
+  p.k = shape->k;
+  p.err = at<int>(ws, L.err);
+  return cuda_status(launch_router_tc_filter(p, at<void>(ws, L.rt_scratch), approx, static_cast<cudaStream_t>(stream)));
+}
+
 unsigned long long moe_kernel_launches(void) { return launch_count().load(std::memory_order_relaxed); }
 
 moe_status_t moe_get_device_error(void* ws, void* stream) {

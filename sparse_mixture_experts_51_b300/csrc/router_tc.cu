@@ -294,4 +294,22 @@ cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t 
   return launch_pdl(router_tc_rank_kernel<4>, dim3(grid), dim3(256), 0, st, 1, p, approx, wt, cn);
 }
 
+// The filter alone (for tests): the weight split and the filter GEMM, the
+// approximate logits g~ [T, nc] written to `approx`.
+cudaError_t launch_router_tc_filter(const RouterParams& p, void* scratch, float* approx, cudaStream_t st) {
+  const int nc = p.W_n ? 2 * p.E : p.E;
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  char* base = static_cast<char*>(scratch);
+  base += up(sizeof(float) * static_cast<size_t>(p.T) * 2 * p.E);
+  __nv_bfloat16* wsplit = reinterpret_cast<__nv_bfloat16*>(base);
+  base += up(2 * static_cast<size_t>(2 * p.E) * 2 * p.d);
+  float* wt = reinterpret_cast<float*>(base);
+  base += up(sizeof(float) * static_cast<size_t>(2 * p.E) * p.d);
+  float* cn = reinterpret_cast<float*>(base);
+  cudaError_t e = launch_pdl(router_tc_prep_kernel, dim3(static_cast<unsigned>(nc)), dim3(256), 0, st, 1, p.W_g,
+                             p.W_n, p.d, p.E, wsplit, wt, cn);
+  if (e != cudaSuccess) return e;
+  return launch_dense_wrapped_gemm(p.x, p.T, p.d, wsplit, nc, 2 * p.d, approx, p.err, st);
+}
+
 }  // namespace moe

@@ -438,7 +438,10 @@ cudaError_t launch_typed(const RouterParams& p, cudaStream_t st, int sms, int ma
   q.nch = (p.d + DK - 1) / DK;
   // narrow tables (CQ <= 4) have the largest token tiles: keep them within portable clusters
   const int ks_max = std::min(CQ <= 4 ? 8 : max_cluster, q.nch);
-  const long long target = 2LL * sms;
+  // CTAs to aim for: two per SM, or (when the next kernel is meant to run
+  // beside this one: the decode-sized layer's expert FFN streams weights
+  // while the routing runs) a single cluster's worth, leaving the other SMs free
+  const long long target = p.early_trigger ? kMaxCluster : 2LL * sms;
 
   // the largest register tile (tokens per thread) that still fills the GPU
   // with at most ks_max CTAs per tile; at most 256 tokens per tile
