@@ -7,7 +7,8 @@ One step = one whole layer forward (router, top-k, capacity dispatch + gather,
 expert GEMMs, combine) over one batch of seeded synthetic tokens already
 resident in HBM, issued through the C ABI (moe_forward_timed).  The timed
 steps are replayed as CUDA graphs (--eager: launched from the host); L2 is
-flushed (256 MiB write) between timed steps, outside the measured events.
+flushed (a 256 MiB write, then a 256 MiB read that writes the dirty lines
+back) between timed steps, outside the measured events.
 
 Prints one JSON line for the headline layer (--workload, by default the
 Mixtral-shaped layer: T=16384, d=4096, E=8 top-2, SwiGLU d_ff=14336, no
@@ -406,7 +407,25 @@ def workload_config(w):
             "noisy_gating": w.noisy, "dtype": w.dtype_name, "seed": w.seed,
             **({"shared_experts": w.n_shared, "d_ff_shared_each": w.F_shared} if w.n_shared else {}),
             **({"routing": "expert_choice"} if w.routing == "expert" else {}),
-            "l2": "flushed between timed steps (256 MiB write, outside the timed events)"}
+            "l2": "flushed between timed steps (256 MiB write then 256 MiB read, outside the timed events)"}
+
+
+class L2Flush:
+    """Empties L2 between timed steps, outside their events: writes a buffer
+    larger than L2, then reads a second one, so that the dirty lines the write
+    leaves are written back here and not during the next step (whose weight
+    stream would otherwise pay for about one L2 of write-backs)."""
+
+    def __init__(self, dev, nbytes=FLUSH_BYTES):
+        import torch
+        self.w = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(nbytes // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        import torch
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
 
 
 class DeviceLayer:
@@ -516,7 +535,7 @@ def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=None, samp
             gr = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gr):
                 for i in range(n):
-                    flush.zero_()
+                    flush()
                     L.forward_timed(evs[i])
             torch.cuda.synchronize()
             graphs[n] = gr
@@ -532,7 +551,7 @@ def time_steps(L, steps, flush, eager=False, slots=TIMED_SLOTS, spans=None, samp
         for n in chunks:
             if eager:
                 for i in range(n):
-                    flush.zero_()
+                    flush()
                     L.forward_timed(evs[i])
             else:
                 graphs[n].replay()
@@ -769,7 +788,7 @@ def shared_ffn_of(L, flush, peaks):
     n = 50
     hev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     for i in range(n):
-        flush.zero_()
+        flush()
         hev[i][0].record(stream)
         call()
         hev[i][1].record(stream)
@@ -799,7 +818,7 @@ def measure(L, a, flush, peaks, steps, e2e_steps, world=1, sampler_index=0, barr
     w = L.w
     for _ in range(max(3, a.warmup)):
         L.forward()
-        flush.zero_()
+        flush()
     torch.cuda.synchronize()
     if L.device_error() != 0:
         raise RuntimeError(f"{w.name}: device-side error in the warm-up")
@@ -863,7 +882,7 @@ def run_ours(a):
     dev = torch.device("cuda", local)
     lib = _lib.load()
     peaks = load_peaks()
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     w = replica_workload(W.WORKLOADS[a.workload], rank, world)
     L = DeviceLayer(w, dev, lib)

@@ -60,6 +60,7 @@ constexpr int TMEM_COLS = NACC * ACC_COLS;
 constexpr int NTHREADS = 384;
 constexpr int EPI_WARPS = 8;
 constexpr int QN = 4;  // tile-queue slots (claimed tiles handed from the producer to the other roles)
+
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 512 /*barriers, queue*/;
 
 struct DecodeArgs {
@@ -75,8 +76,20 @@ struct DecodeArgs {
   const int32_t* offsets;
   float* y;        // [rows, d]
   long long rows;  // allocated rows of y
-  int* ctrl;       // [0] ticket, [1] finished CTAs, [2, 2+E) finished phase-1 epilogue warps per expert
+  int* ctrl;       // [0] ticket, [1] finished CTAs, [2, 2+E) finished phase-1 epilogue warps per expert,
+                   // [2+E, 2+E+n2) finished phase-2 epilogue warps per 256-column block
   int* err;
+  // the combine (residual + gated sum over the token's kept ranks, in rank order, + shared experts)
+  const __nv_bfloat16* x_res;  // [T, d] residual (the tokens)
+  const float* w;              // [T, k] gates
+  const float* y_shared;       // [T, d] fp32 or null
+  __nv_bfloat16* out;          // [T, d]
+  float* moe_out;              // [T, d] fp32 or null
+  // the same weights as plain pointers, for the L2 prefetch of each CTA's first tile
+  const __nv_bfloat16* W1;
+  const __nv_bfloat16* W3;
+  const __nv_bfloat16* W2;
+  int pf_bytes_row;  // bytes of every weight row of its first tile that a CTA prefetches into L2
 };
 
 __device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
@@ -109,6 +122,82 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The combine of one 256-column block (the standalone combine's arithmetic,
+// so the layer output is the same bit for bit): per token t and 16-element
+// chunk, acc = fma over the kept ranks r = 0..k-1 of w[t,r] * y[row(t,r)],
+// + the shared experts' output, out = bf16(x + acc), moe_out = acc.
+// Threads `tid` of `nthr` take (token, chunk) items in turn.
+__device__ __forceinline__ void combine_block(const DecodeArgs& g, int cb, int tid, int nthr) {
+  const int chunks = BN / 16;
+  for (int it = tid; it < g.T * chunks; it += nthr) {
+    const int t = it / chunks;
+    const int c = cb * BN + (it - t * chunks) * 16;
+    if (c >= g.d) continue;
+    const long long base = static_cast<long long>(t) * g.d + c;
+    float rv[16];
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(g.x_res + base);
+      const uint4 a = __ldcg(src), b = __ldcg(src + 1);
+      const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        rv[2 * i] = __uint_as_float(u[i] << 16);
+        rv[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
+      }
+    }
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+    for (int r = 0; r < g.k; ++r) {
+      const long long a = static_cast<long long>(t) * g.k + r;
+      const int ps = __ldcg(g.pos + a);
+      if (ps < 0) continue;  // dropped: the residual carries the token
+      const int e = __ldcg(g.idx + a);
+      long long row = -1;
+      if (e >= 0 && e < g.E) row = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
+      if (row < 0 || row >= g.rows) {
+        record_error(g.err, MOE_ERR_BOUNDS);
+        continue;
+      }
+      const float wt = __ldcg(g.w + a);
+      const float4* ysrc = reinterpret_cast<const float4*>(g.y + row * g.d + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = __ldcg(ysrc + q);
+        acc[4 * q] = fmaf(wt, v.x, acc[4 * q]);
+        acc[4 * q + 1] = fmaf(wt, v.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(wt, v.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(wt, v.w, acc[4 * q + 3]);
+      }
+    }
+    if (g.y_shared) {
+      const float4* ssrc = reinterpret_cast<const float4*>(g.y_shared + base);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 v = __ldcg(ssrc + q);
+        acc[4 * q] += v.x;
+        acc[4 * q + 1] += v.y;
+        acc[4 * q + 2] += v.z;
+        acc[4 * q + 3] += v.w;
+      }
+    }
+    if (g.moe_out) {
+      float4* mo = reinterpret_cast<float4*>(g.moe_out + base);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mo[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+    }
+    uint32_t pk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(rv[2 * i] + acc[2 * i], rv[2 * i + 1] + acc[2 * i + 1]);
+      pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(g.out + base);
+    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  }
+}
+
 __global__ void __launch_bounds__(NTHREADS, 1)
     ffn_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                       const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmH,
@@ -130,10 +219,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int E = g.E;
   const int total1 = E * g.n1;
-  const int total = total1 + E * g.n2;
+  const int total12 = total1 + E * g.n2;
+  const int total = total12 + g.n2;  // then one combine tile per 256-column block
   int* ticket = g.ctrl;
   int* finished = g.ctrl + 1;
   int* done1 = g.ctrl + 2;
+  int* done2 = done1 + E;
   const int done_target = EPI_WARPS * g.n1;
 
   if (tid == 0) {
@@ -188,7 +279,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           while (true) {
             id = atomicAdd(ticket, 1);
             if (id >= total) { id = -1; break; }
-            if (id < total1) break;
+            if (id < total1 || id >= total12) break;
             if (!routed) {
               pdl_wait();  // the routing tables are complete from here on
               routed = true;
@@ -203,6 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(smem_u32(&qfull[q]));
         if (++q == QN) { q = 0; qphase ^= 1u; }
         if (id < 0) break;
+        if (id >= total12) continue;  // a combine tile: no loads
 
         const bool p1 = id < total1;
         const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
@@ -287,6 +379,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(smem_u32(&qempty[q]));
         if (++q == QN) { q = 0; qphase ^= 1u; }
         if (id < 0) break;
+        if (id >= total12) continue;  // a combine tile: no MMA
         const int KB = id < total1 ? g.kb1 : g.kb2;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), aphase ^ 1u, g.err, abort_flag)) break;
         tc_fence_after();
@@ -325,6 +418,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     int q = 0;
     uint32_t qphase = 0;
     bool routed = false;
+    bool first = true;
     while (true) {
       if (!mbar_wait_bounded(smem_u32(&qfull[q]), qphase, g.err, abort_flag)) break;
       const int id = s_tile[q];
@@ -332,16 +426,85 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&qempty[q]));
       if (++q == QN) { q = 0; qphase ^= 1u; }
       if (id < 0) break;
-      const bool p1 = id < total1;
-      const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
-      const int nb = p1 ? id - e * g.n1 : (id - total1) - e * g.n2;
-      // phase 2: the grouped row this token's assignment to e was given (-1: none or dropped)
-      long long dest = -1;
-      if (!p1) {
+      if (id >= total12) {
+        // ---- combine tile: columns [cb*256, cb*256+256) of every token, once
+        // every active expert's phase-2 tile of that block has stored its rows
+        const int cb = id - total12;
         if (!routed) {
           pdl_wait();
           routed = true;
         }
+        int n_active = 0;
+        for (int e2 = lane; e2 < E; e2 += 32) n_active += __ldcg(g.offsets + e2 + 1) > __ldcg(g.offsets + e2) ? 1 : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n_active += __shfl_xor_sync(0xffffffffu, n_active, o);
+        bool ready = true;
+        if (lane == 0) {
+          const unsigned long long t0 = globaltimer_ns();
+          while (ld_acquire(done2 + cb) < EPI_WARPS * n_active) {
+            if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+              record_error(g.err, MOE_ERR_DEVICE_TIMEOUT);
+              *abort_flag = 1;
+              ready = false;
+              break;
+            }
+          }
+        }
+        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+        if (!ready) break;
+        (void)ld_acquire(done2 + cb);  // every lane's reads below follow the completed count
+        combine_block(g, cb, (warp - 4) * 32 + lane, EPI_WARPS * 32);
+        continue;
+      }
+      const bool p1 = id < total1;
+      const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
+      const int nb = p1 ? id - e * g.n1 : (id - total1) - e * g.n2;
+      if (first) {
+        // The kernel was launched while the routing kernels still run, and
+        // the hardware holds tensor-map TMA loads of a kernel launched that
+        // way until the kernel before it completes; plain loads are not
+        // held.  So while the first tile's TMA loads wait, the idle epilogue
+        // warps request the leading part of its weight rows into L2 (the
+        // loads find them there once they are released).
+        first = false;
+        const char* base;
+        int nrows;
+        long long row_bytes;
+        if (p1) {
+          row_bytes = static_cast<long long>(g.d) * 2;
+          nrows = g.swiglu ? 128 : BN;
+          base = reinterpret_cast<const char*>(g.W1) + (static_cast<long long>(e) * g.F + nb * nrows) * row_bytes;
+        } else {
+          row_bytes = static_cast<long long>(g.F) * 2;
+          nrows = BN;
+          base = reinterpret_cast<const char*>(g.W2) + (static_cast<long long>(e) * g.d + nb * BN) * row_bytes;
+        }
+        const int lines = g.pf_bytes_row / 128;
+        const int et = (warp - 4) * 32 + lane;
+        const int last_row = p1 ? (g.E * g.F) : (g.E * g.d);  // rows of the weight tensor
+        const int row0 = p1 ? e * g.F + nb * nrows : e * g.d + nb * BN;
+        for (int i = et; i < nrows * lines; i += EPI_WARPS * 32) {
+          const int r = i / lines, l = i - r * lines;
+          if (row0 + r >= last_row) continue;
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + r * row_bytes + l * 128));
+          if (p1 && g.swiglu) {
+            const char* b3 = reinterpret_cast<const char*>(g.W3) + (static_cast<long long>(e) * g.F + nb * 128) * row_bytes;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(b3 + r * row_bytes + l * 128));
+          }
+        }
+      }
+      // The routing tables are read from here on.  Waiting for the routing
+      // kernels costs nothing at this point: the accumulator this warp is
+      // about to drain holds data of TMA loads, and those are released only
+      // once the kernel before this one has completed.
+      if (!routed) {
+        pdl_wait();
+        routed = true;
+      }
+      // the grouped row of this token's kept assignment to e (-1: none or dropped);
+      // phase 1 stores only the hidden rows phase 2 will scatter
+      long long dest = -1;
+      {
         if (t < g.T) {
           for (int r = 0; r < g.k; ++r) {
             const long long a = static_cast<long long>(t) * g.k + r;
@@ -375,7 +538,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tmem_wait_ld(gr, ur);
           if (c == half * 2 + 1) release();
           const int col = nb * 128 + c * 32;
-          if (col < g.F) {
+          if (col < g.F && dest >= 0) {
             uint4 pk[4];
             __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
@@ -402,7 +565,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int col = nb * BN + (c + j) * 32;
             if (p1) {
               // GELU: h = gelu(a + b1)
-              if (col < g.F) {
+              if (col < g.F && dest >= 0) {
                 const float* bias = g.b1 ? g.b1 + static_cast<long long>(e) * g.F + col : nullptr;
                 uint4 pk[4];
                 __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
@@ -434,13 +597,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (p1) {
-        // this warp's rows of the tile are stored: count it for expert e (the
-        // phase-2 tiles of e read these rows through TMA after the count is complete)
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) atomicAdd(done1 + e, 1);
-      }
+      // this warp's rows of the tile are stored: count it, for expert e (its
+      // phase-2 tiles read these hidden rows through TMA once the count is
+      // complete) or for the column block (its combine tile reads these rows)
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) atomicAdd(p1 ? done1 + e : done2 + nb, 1);
       if (++acc == NACC) { acc = 0; aphase ^= 1u; }
     }
   }
@@ -455,7 +617,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __threadfence();
     if (atomicAdd(finished, 1) == static_cast<int>(gridDim.x) - 1) {
       *ticket = 0;
-      for (int e = 0; e < E; ++e) done1[e] = 0;
+      for (int e = 0; e < E + g.n2; ++e) done1[e] = 0;  // and done2, which follows
       __threadfence();
       *finished = 0;
       __threadfence();
@@ -508,7 +670,9 @@ bool ffn_decode_applies(const moe_shape_t& s) {
 }
 
 size_t ffn_decode_h_bytes(const moe_shape_t& s) { return static_cast<size_t>(s.E) * BM * s.d_ff * 2; }
-size_t ffn_decode_ctrl_bytes(const moe_shape_t& s) { return sizeof(int) * (2 + static_cast<size_t>(s.E)); }
+size_t ffn_decode_ctrl_bytes(const moe_shape_t& s) {
+  return sizeof(int) * (2 + static_cast<size_t>(s.E) + static_cast<size_t>((s.d + BN - 1) / BN));
+}
 
 cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st) {
   cudaError_t e = get_encoder();
@@ -548,11 +712,25 @@ cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st) {
   g.rows = p.rows;
   g.ctrl = p.ctrl;
   g.err = p.err;
+  g.W1 = static_cast<const __nv_bfloat16*>(p.W1);
+  g.W3 = static_cast<const __nv_bfloat16*>(p.W3);
+  g.W2 = static_cast<const __nv_bfloat16*>(p.W2);
+  g.x_res = static_cast<const __nv_bfloat16*>(p.x);
+  g.w = p.w;
+  g.y_shared = p.y_shared;
+  g.out = static_cast<__nv_bfloat16*>(p.out);
+  g.moe_out = p.moe_out;
   if ((e = cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
       cudaSuccess)
     return e;
-  const long long tiles = static_cast<long long>(p.E) * (g.n1 + g.n2);
+  const long long tiles = static_cast<long long>(p.E) * (g.n1 + g.n2) + g.n2;
   const int grid = static_cast<int>(std::min<long long>(sms, tiles));
+  // the first-tile L2 prefetch: at most kPrefetchBudget bytes over all CTAs
+  // (well inside L2), whole 128-byte lines of every row of the tile's panel
+  constexpr long long kPrefetchBudget = 80LL << 20;
+  const long long tile_rows = swiglu ? 256 : BN;
+  const long long per_row = kPrefetchBudget / grid / tile_rows;
+  g.pf_bytes_row = static_cast<int>(std::min<long long>(static_cast<long long>(std::min(p.d, p.F)) * 2, per_row) / 128 * 128);
   NvtxRange r("expert_ffn_decode");
   return launch_pdl(ffn_decode_kernel, dim3(grid), dim3(NTHREADS), static_cast<size_t>(SMEM_BYTES), st, 1, mX, mW1,
                     mW3, mH, mW2, g);

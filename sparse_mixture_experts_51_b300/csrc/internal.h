@@ -219,9 +219,10 @@ struct FfnParams {
   long long rows;  // allocated rows of x_perm / h / y_perm
   int* err;
 };
-// The expert FFN of a decode-sized batch (ffn_decode.cu): one persistent
-// kernel, phase 1 dense over all T <= 128 tokens (no routing needed), phase 2
-// scattered to the kept assignments' grouped rows of y_perm.
+// The expert FFN and combine of a decode-sized batch (ffn_decode.cu): one
+// persistent kernel, phase 1 dense over all T <= 128 tokens (no routing
+// needed), phase 2 scattered to the kept assignments' grouped rows of
+// y_perm, then the weighted combine into the residual, block by block.
 struct DecodeFfnParams {
   const void* x;  // [T, d] bf16 tokens
   int T, d, F, E, k, act;
@@ -236,8 +237,13 @@ struct DecodeFfnParams {
   const int32_t* offsets;
   float* y_perm;           // [rows, d]
   long long rows;
-  int* ctrl;               // 2 + E ints, zero at first use (self-resetting)
+  int* ctrl;               // ffn_decode_ctrl_bytes, zero at first use (self-resetting)
   int* err;
+  // the combine, done by the same kernel: out = x + sum over kept ranks of w * y (+ y_shared)
+  const float* w;          // [T,k] gates
+  const float* y_shared;   // [T,d] fp32 or null
+  void* out;               // [T,d] bf16
+  float* moe_out;          // [T,d] fp32 or null
 };
 bool ffn_decode_applies(const moe_shape_t& s);
 size_t ffn_decode_h_bytes(const moe_shape_t& s);

@@ -677,9 +677,15 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     dp.rows = L.rows;
     dp.ctrl = at<int>(ws, L.dec_ctrl);
     dp.err = at<int>(ws, L.err);
+    dp.w = w;
+    dp.y_shared = y_sh;
+    dp.out = out;
+    dp.moe_out = moe_out;
     if ((st = cuda_status(launch_ffn_decode(dp, s))) != MOE_OK) return st;
+    // the same kernel did the combine: stage events 3, 4 and 5 all follow it
     if ((st = mark(3)) != MOE_OK) return st;
-    row_of = nullptr;  // no gather wrote it: the combine finds the rows from idx, pos and offsets
+    if ((st = mark(4)) != MOE_OK) return st;
+    return mark(5);
   } else if (shape->dtype == MOE_BF16) {
     // launch_ffn_bf16 names its two GEMMs (expert_gemm1, expert_gemm2) itself
     if ((st = cuda_status(launch_ffn_bf16(fp, s, stage_events ? static_cast<cudaEvent_t>(stage_events[3]) : nullptr))) != MOE_OK)

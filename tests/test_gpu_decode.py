@@ -107,7 +107,7 @@ def test_decode_layer_with_rerouting():
 
 
 def test_decode_kernel_count():
-    """router, dispatch, one fused expert-FFN kernel, combine: four launches."""
+    """router, dispatch and one kernel for both expert GEMMs and the combine: three launches."""
     from sparse_mixture_experts_51_b300 import _lib
 
     lib = _lib.load()
@@ -120,4 +120,29 @@ def test_decode_kernel_count():
     n0 = lib.moe_kernel_launches()
     layer(g["x"])
     torch.cuda.synchronize()
-    assert lib.moe_kernel_launches() - n0 == 4
+    assert lib.moe_kernel_launches() - n0 == 3
+
+
+def test_decode_layer_with_shared_experts():
+    """A decode-sized layer with a shared expert: the fused kernel's combine
+    adds the shared experts' output after the routed ranks, as the standalone
+    combine does."""
+    from _parity import shared_args
+
+    w = W.Workload("dec_shared", T=64, d=256, E=16, k=2, F=256, act=W.ACT_SWIGLU, capacity_factor=1.5,
+                   dtype=torch.bfloat16, seed=87, n_shared=1, F_shared=256)
+    inp = W.make_inputs(w)
+    g = to_gpu(inp)
+    gpu = gpu_forward(w, g)
+    ref = oracle_forward(w, inp)
+    check_layer(w, inp, gpu, ref)
+    C = api.capacity(w.T, w.k, w.E, w.capacity_factor)
+    idx, wt, _ = api.route(g["x"], g["W_g"], w.k)
+    d = api.dispatch(idx, g["x"], w.E, C, d_ff=w.F, act="swiglu")
+    y = api.expert_ffn(d["x_perm"], d["offsets"], g["W1"], g["W2"], w.T, w.k, C, "swiglu", W3=g["W3"])
+    ys = api.shared_ffn(g["x"], act="swiglu", **shared_args(g))
+    out, moe = api.combine(y, idx, wt, d["pos"], d["offsets"], g["x"], w.E, C, w.dtype, d_ff=w.F, want_moe=True,
+                           y_shared=ys)
+    torch.cuda.synchronize()
+    assert torch.equal(gpu["out"], out.cpu())
+    assert torch.equal(gpu["moe"], moe.cpu())
