@@ -1,5 +1,5 @@
-// Expert FFN of a decode-sized batch (T <= 128 tokens) as one persistent
-// tcgen05 kernel whose first phase does not wait for the routing.
+// Expert FFN and combine of a decode-sized batch (T <= 128 tokens) as one
+// persistent tcgen05 kernel whose first phase does not need the routing.
 //
 // With T <= 128 every expert's rows fit one 128-row M tile, so computing an
 // expert over ALL T tokens costs the tensor cores exactly what computing it
@@ -7,36 +7,44 @@
 // depends only on its own input row: the rows of the kept (token, expert)
 // pairs come out bit for bit as the grouped GEMMs give them.  The layer is
 // then a stream of expert weights (SwiGLU: 3 d F bytes per expert, GELU:
-// 2 d F), and the stream can start before the router has finished:
+// 2 d F):
 //
-//   phase 1  h_all[e*128 + t] = act(x[t] W1[e]^T (, x[t] W3[e]^T)) for every
-//            expert e and token t < T (rows t >= T are zero-filled by TMA and
-//            never read back); one tile = expert e x 128 (SwiGLU) or 256
-//            (GELU) columns of h, A = the token matrix itself
-//   phase 2  y_perm[offsets[e] + pos[t,r]] = h_all[e*128 + t] W2[e]^T + b2[e]
+//   phase 1  h[e*128 + t] = act(x[t] W1[e]^T (, x[t] W3[e]^T)) for every
+//            expert e and token t < T (the tile's rows t >= T read zeros);
+//            one tile = expert e x 128 (SwiGLU) or 256 (GELU) columns of h,
+//            A = the token matrix itself; only the rows of kept (t, e)
+//            pairs are stored
+//   phase 2  y_perm[offsets[e] + pos[t,r]] = h[e*128 + t] W2[e]^T + b2[e]
 //            for every kept assignment (t, r) of expert e: the epilogue
-//            scatters each row to its grouped row (the combine's layout),
-//            other rows are not stored; one tile = expert e x 256 columns
+//            scatters each row to its grouped row, other rows are not
+//            stored; one tile = expert e x 256 columns
+//   combine  out[t] = x[t] + sum over t's kept ranks r (in order) of
+//            w[t,r] y_perm[row(t,r)] (+ the shared experts' output); one
+//            tile = 16 tokens x 256 columns
 //
 // (the expert FFN of "Mixture-of-Experts Sparse Model Scaling", Core
-// Concepts; a dropped assignment skips its expert as in "LLM part 09", s3:
-// its row is computed but never stored or combined).
+// Concepts; y = sum_i G(x)_i E_i(x) of "LLM part 09", s1; a dropped
+// assignment skips its expert as in s3: its row is computed but never
+// stored or combined).
 //
 // Tiles are claimed one at a time from a ticket in the workspace: every
-// phase-1 tile before every phase-2 tile, experts in order.  A phase-2 tile
-// of expert e waits until all phase-1 tiles of e have stored their rows (a
-// per-expert count of finished epilogue warps).  Every tile a CTA waits on
-// was claimed earlier by a CTA that is running and does not wait on
-// anything later, so the waits always end.  The routing tables (idx, pos,
-// offsets) are read only after griddepcontrol.wait; a phase-2 tile of an
-// expert without kept rows is skipped.  The last CTA to finish clears the
-// ticket and counts for the next call.
+// phase-1 tile, then every phase-2 tile (experts in order), then the
+// combine tiles.  A phase-2 tile of expert e waits until all phase-1 tiles
+// of e have stored their rows, and a combine tile until every active
+// expert's phase-2 tile of its column block has (counts of finished
+// epilogue warps).  Every tile a CTA waits on was claimed earlier by a CTA
+// that is running and does not wait on anything later, so the waits always
+// end.  The routing tables (idx, pos, offsets, w) are read only after
+// griddepcontrol.wait; a phase-2 tile of an expert without kept rows is
+// skipped.  The last CTA to finish clears the ticket and counts for the
+// next call.
 //
 // Roles per CTA (384 threads): warp 0 claims tiles and issues TMA loads
 // (4-stage ring of 48 KB: A 128x64, B 256x64, 128-byte swizzle); warp 1
 // issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators;
 // warp 2 owns TMEM; warps 4-11 drain the accumulator (two per TMEM lane
-// quarter, half of the 32-column chunks each) with whole-sector stores.
+// quarter, half of the 32-column chunks each) with whole-sector stores, and
+// run the combine tiles (one (token, 16-column chunk) item per thread).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -122,80 +130,92 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// The combine of one 256-column block (the standalone combine's arithmetic,
-// so the layer output is the same bit for bit): per token t and 16-element
-// chunk, acc = fma over the kept ranks r = 0..k-1 of w[t,r] * y[row(t,r)],
-// + the shared experts' output, out = bf16(x + acc), moe_out = acc.
-// Threads `tid` of `nthr` take (token, chunk) items in turn.
-__device__ __forceinline__ void combine_block(const DecodeArgs& g, int cb, int tid, int nthr) {
-  const int chunks = BN / 16;
-  for (int it = tid; it < g.T * chunks; it += nthr) {
-    const int t = it / chunks;
-    const int c = cb * BN + (it - t * chunks) * 16;
-    if (c >= g.d) continue;
-    const long long base = static_cast<long long>(t) * g.d + c;
-    float rv[16];
-    {
-      const uint4* src = reinterpret_cast<const uint4*>(g.x_res + base);
-      const uint4 a = __ldcg(src), b = __ldcg(src + 1);
-      const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+// The combine of 16 tokens x one 256-column block (the standalone combine's
+// arithmetic, so the layer output is the same bit for bit): per token t and
+// 16-element chunk, acc = fma over the kept ranks r = 0..k-1 of
+// w[t,r] * y[row(t,r)], + the shared experts' output, out = bf16(x + acc),
+// moe_out = acc.  One (token, chunk) item per thread; the loads of every
+// rank are issued before the sums so their latencies overlap.
+constexpr int COMBINE_TOKENS = 16;
+__device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg, int item) {
+  const int t = tg * COMBINE_TOKENS + item / (BN / 16);
+  const int c = cb * BN + (item % (BN / 16)) * 16;
+  if (t >= g.T || c >= g.d) return;
+  const long long base = static_cast<long long>(t) * g.d + c;
+  long long row[kMaxTopK];
+  float wt[kMaxTopK];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        rv[2 * i] = __uint_as_float(u[i] << 16);
-        rv[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
-      }
-    }
-    float acc[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-    for (int r = 0; r < g.k; ++r) {
+  for (int r = 0; r < kMaxTopK; ++r) {
+    row[r] = -1;
+    wt[r] = 0.f;
+    if (r < g.k) {
       const long long a = static_cast<long long>(t) * g.k + r;
       const int ps = __ldcg(g.pos + a);
-      if (ps < 0) continue;  // dropped: the residual carries the token
       const int e = __ldcg(g.idx + a);
-      long long row = -1;
-      if (e >= 0 && e < g.E) row = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
-      if (row < 0 || row >= g.rows) {
-        record_error(g.err, MOE_ERR_BOUNDS);
-        continue;
-      }
-      const float wt = __ldcg(g.w + a);
-      const float4* ysrc = reinterpret_cast<const float4*>(g.y + row * g.d + c);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = __ldcg(ysrc + q);
-        acc[4 * q] = fmaf(wt, v.x, acc[4 * q]);
-        acc[4 * q + 1] = fmaf(wt, v.y, acc[4 * q + 1]);
-        acc[4 * q + 2] = fmaf(wt, v.z, acc[4 * q + 2]);
-        acc[4 * q + 3] = fmaf(wt, v.w, acc[4 * q + 3]);
+      wt[r] = __ldcg(g.w + a);
+      if (ps >= 0) {  // dropped: the residual carries the token
+        if (e >= 0 && e < g.E) row[r] = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
+        if (row[r] < 0 || row[r] >= g.rows) {
+          record_error(g.err, MOE_ERR_BOUNDS);
+          row[r] = -1;
+        }
       }
     }
-    if (g.y_shared) {
-      const float4* ssrc = reinterpret_cast<const float4*>(g.y_shared + base);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = __ldcg(ssrc + q);
-        acc[4 * q] += v.x;
-        acc[4 * q + 1] += v.y;
-        acc[4 * q + 2] += v.z;
-        acc[4 * q + 3] += v.w;
-      }
-    }
-    if (g.moe_out) {
-      float4* mo = reinterpret_cast<float4*>(g.moe_out + base);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) mo[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-    }
-    uint32_t pk[8];
+  }
+  float rv[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(g.x_res + base);
+    const uint4 a = __ldcg(src), b = __ldcg(src + 1);
+    const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const __nv_bfloat162 h2 = __floats2bfloat162_rn(rv[2 * i] + acc[2 * i], rv[2 * i + 1] + acc[2 * i + 1]);
-      pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      rv[2 * i] = __uint_as_float(u[i] << 16);
+      rv[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
     }
-    uint4* dst = reinterpret_cast<uint4*>(g.out + base);
-    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   }
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll 4
+  for (int r = 0; r < g.k; ++r) {
+    if (row[r] < 0) continue;
+    const float4* ysrc = reinterpret_cast<const float4*>(g.y + row[r] * g.d + c);
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldcg(ysrc + q);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[4 * q] = fmaf(wt[r], v[q].x, acc[4 * q]);
+      acc[4 * q + 1] = fmaf(wt[r], v[q].y, acc[4 * q + 1]);
+      acc[4 * q + 2] = fmaf(wt[r], v[q].z, acc[4 * q + 2]);
+      acc[4 * q + 3] = fmaf(wt[r], v[q].w, acc[4 * q + 3]);
+    }
+  }
+  if (g.y_shared) {
+    const float4* ssrc = reinterpret_cast<const float4*>(g.y_shared + base);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = __ldcg(ssrc + q);
+      acc[4 * q] += v.x;
+      acc[4 * q + 1] += v.y;
+      acc[4 * q + 2] += v.z;
+      acc[4 * q + 3] += v.w;
+    }
+  }
+  if (g.moe_out) {
+    float4* mo = reinterpret_cast<float4*>(g.moe_out + base);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mo[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  }
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(rv[2 * i] + acc[2 * i], rv[2 * i + 1] + acc[2 * i + 1]);
+    pk[i] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(g.out + base);
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -220,7 +240,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int E = g.E;
   const int total1 = E * g.n1;
   const int total12 = total1 + E * g.n2;
-  const int total = total12 + g.n2;  // then one combine tile per 256-column block
+  const int n_tg = (g.T + COMBINE_TOKENS - 1) / COMBINE_TOKENS;
+  const int total = total12 + g.n2 * n_tg;  // then one combine tile per 256-column block and 16 tokens
   int* ticket = g.ctrl;
   int* finished = g.ctrl + 1;
   int* done1 = g.ctrl + 2;
@@ -294,7 +315,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(smem_u32(&qfull[q]));
         if (++q == QN) { q = 0; qphase ^= 1u; }
         if (id < 0) break;
-        if (id >= total12) continue;  // a combine tile: no loads
+        if (id >= total12) {
+          // a combine tile needs no loads; a CTA takes one at most (when the
+          // grid has a CTA for each), so they run side by side
+          if (static_cast<int>(gridDim.x) >= total - total12) ok = false;
+          continue;
+        }
 
         const bool p1 = id < total1;
         const int e = p1 ? id / g.n1 : (id - total1) / g.n2;
@@ -427,9 +453,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (++q == QN) { q = 0; qphase ^= 1u; }
       if (id < 0) break;
       if (id >= total12) {
-        // ---- combine tile: columns [cb*256, cb*256+256) of every token, once
+        // ---- combine tile: columns [cb*256, cb*256+256) of 16 tokens, once
         // every active expert's phase-2 tile of that block has stored its rows
-        const int cb = id - total12;
+        const int cb = (id - total12) / n_tg, tg = (id - total12) - cb * n_tg;
         if (!routed) {
           pdl_wait();
           routed = true;
@@ -453,7 +479,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
         if (!ready) break;
         (void)ld_acquire(done2 + cb);  // every lane's reads below follow the completed count
-        combine_block(g, cb, (warp - 4) * 32 + lane, EPI_WARPS * 32);
+        static_assert(COMBINE_TOKENS * (BN / 16) == EPI_WARPS * 32, "one combine item per epilogue thread");
+        combine_item(g, cb, tg, (warp - 4) * 32 + lane);
         continue;
       }
       const bool p1 = id < total1;
@@ -462,10 +489,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (first) {
         // The kernel was launched while the routing kernels still run, and
         // the hardware holds tensor-map TMA loads of a kernel launched that
-        // way until the kernel before it completes; plain loads are not
-        // held.  So while the first tile's TMA loads wait, the idle epilogue
-        // warps request the leading part of its weight rows into L2 (the
-        // loads find them there once they are released).
+        // way until the kernel before it completes.  While the first tile's
+        // loads wait, the idle epilogue warps request the leading part of
+        // its weight rows into L2 (one bulk prefetch per row).
         first = false;
         const char* base;
         int nrows;
@@ -479,17 +505,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           nrows = BN;
           base = reinterpret_cast<const char*>(g.W2) + (static_cast<long long>(e) * g.d + nb * BN) * row_bytes;
         }
-        const int lines = g.pf_bytes_row / 128;
         const int et = (warp - 4) * 32 + lane;
         const int last_row = p1 ? (g.E * g.F) : (g.E * g.d);  // rows of the weight tensor
         const int row0 = p1 ? e * g.F + nb * nrows : e * g.d + nb * BN;
-        for (int i = et; i < nrows * lines; i += EPI_WARPS * 32) {
-          const int r = i / lines, l = i - r * lines;
+        for (int r = et; r < nrows; r += EPI_WARPS * 32) {
           if (row0 + r >= last_row) continue;
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(base + r * row_bytes + l * 128));
+          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base + r * row_bytes), "r"(g.pf_bytes_row)
+                       : "memory");
           if (p1 && g.swiglu) {
             const char* b3 = reinterpret_cast<const char*>(g.W3) + (static_cast<long long>(e) * g.F + nb * 128) * row_bytes;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(b3 + r * row_bytes + l * 128));
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b3 + r * row_bytes), "r"(g.pf_bytes_row)
+                         : "memory");
           }
         }
       }
@@ -723,10 +749,10 @@ cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st) {
   if ((e = cudaFuncSetAttribute(ffn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) !=
       cudaSuccess)
     return e;
-  const long long tiles = static_cast<long long>(p.E) * (g.n1 + g.n2) + g.n2;
+  const long long tiles = static_cast<long long>(p.E) * (g.n1 + g.n2) + static_cast<long long>(g.n2) * ((p.T + 15) / 16);
   const int grid = static_cast<int>(std::min<long long>(sms, tiles));
   // the first-tile L2 prefetch: at most kPrefetchBudget bytes over all CTAs
-  // (well inside L2), whole 128-byte lines of every row of the tile's panel
+  // (well inside L2), a multiple of 128 bytes of every row of the tile's panel
   constexpr long long kPrefetchBudget = 80LL << 20;
   const long long tile_rows = swiglu ? 256 : BN;
   const long long per_row = kPrefetchBudget / grid / tile_rows;
