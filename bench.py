@@ -61,7 +61,8 @@ HBM_NOMINAL_GBS = 8000.0
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
 # hash of the kernel sources it was taken on; a changed kernel reports null.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-GEMM_SOURCES = ["sparse_mixture_experts_51_b300/csrc/gemm_tc.cu", "sparse_mixture_experts_51_b300/csrc/common.cuh"]
+GEMM_SOURCES = ["sparse_mixture_experts_51_b300/csrc/gemm_tc.cu", "sparse_mixture_experts_51_b300/csrc/ffn_decode.cu",
+                "sparse_mixture_experts_51_b300/csrc/common.cuh"]
 
 
 def parse_args(argv=None):
