@@ -149,6 +149,16 @@ cudaError_t launch_router(const RouterParams& p, int dtype, cudaStream_t st);
 // the tensor-core filter router (router_tc.cu) for wide logit tables of bf16 layers
 bool router_tc_applies(const RouterParams& p, int dtype);
 size_t router_tc_scratch_bytes(long long T, int d, int E);
+// its carve-up of that scratch: approximate logits [T][nc], the bf16 hi|lo
+// split of the router-weight columns [nc][2d], the fp32 columns [nc][d] and
+// their norms [nc] (nc = E, or 2E with the noise columns)
+struct RouterTcScratch {
+  float* approx;
+  void* wsplit;
+  float* wt;
+  float* cn;
+};
+RouterTcScratch router_tc_scratch(void* scratch, long long T, int d, int E);
 cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t st);
 // its weight split and filter GEMM alone: the approximate logits [T, nc] (a test hook)
 cudaError_t launch_router_tc_filter(const RouterParams& p, void* scratch, float* approx, cudaStream_t st);
@@ -232,20 +242,38 @@ struct DecodeFfnParams {
   const float* b1;
   const float* b2;
   void* h;                 // [E*128, F] bf16 workspace
-  const int32_t* idx;      // [T,k] routing tables (read after the routing kernels complete)
-  const int32_t* pos;
-  const int32_t* offsets;
+  // [T,k] routing tables: read after the routing kernels complete, or (self_route)
+  // written by the kernel's own routing tiles before any tile reads them
+  int32_t* idx;
+  int32_t* pos;
+  int32_t* offsets;
   float* y_perm;           // [rows, d]
   long long rows;
   int* ctrl;               // ffn_decode_ctrl_bytes, zero at first use (self-resetting)
   int* err;
   // the combine, done by the same kernel: out = x + sum over kept ranks of w * y (+ y_shared)
-  const float* w;          // [T,k] gates
+  float* w;                // [T,k] gates (written by the routing tiles when self_route)
   const float* y_shared;   // [T,d] fp32 or null
   void* out;               // [T,d] bf16
   float* moe_out;          // [T,d] fp32 or null
+  // self_route = 1: the kernel also routes (exact top-k as in router.cu) and
+  // dispatches (slots in priority order, capacity C, as in dispatch.cu)
+  int self_route;
+  const float* W_g;
+  const float* b_g;
+  const float* W_n;
+  const float* eps;
+  int gate_raw;
+  int C;
+  float* logits;           // [T,E] or null
+  long long* stats;        // router counters or null
+  int32_t* counts;         // [E]
+  long long* dropped;      // [1]
 };
 bool ffn_decode_applies(const moe_shape_t& s);
+// the fused kernel can also route the batch: overflow drop, nc = E (2E with the
+// noise projection) a power of two in [4, 256], router weights 16-byte aligned
+bool ffn_decode_routes(const moe_shape_t& s, const float* W_g, const float* W_n);
 size_t ffn_decode_h_bytes(const moe_shape_t& s);
 size_t ffn_decode_ctrl_bytes(const moe_shape_t& s);
 cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st);

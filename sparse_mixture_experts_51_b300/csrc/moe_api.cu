@@ -576,6 +576,8 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
   };
   const bool ec = shape->routing == MOE_ROUTE_EXPERT_CHOICE;
   if (ec && (idx != nullptr || w != nullptr || pos != nullptr)) return MOE_ERR_INVALID_ARG;
+  // decode-sized batches whose router fits the fused kernel: one launch for the whole layer
+  const bool self_route = L.dec && !ec && ffn_decode_routes(*shape, W_g, W_noise);
   if (idx == nullptr) idx = at<int32_t>(ws, L.idx);
   if (w == nullptr) w = at<float>(ws, L.w);
   if (pos == nullptr) pos = at<int32_t>(ws, L.pos);
@@ -619,6 +621,9 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     row_of = ep.row_of;
     gate = ep.gate_te;
     cshape.k = shape->E;
+  } else if (self_route) {
+    // the fused decode kernel routes and dispatches the batch itself (its first tiles)
+    if ((st = mark(1)) != MOE_OK) return st;
   } else {
     int32_t* backup = shape->overflow == MOE_OVERFLOW_REROUTE ? at<int32_t>(ws, L.rr_backup) : nullptr;
     // decode-sized batches: the router and the dispatch let the fused expert
@@ -681,6 +686,19 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
     dp.y_shared = y_sh;
     dp.out = out;
     dp.moe_out = moe_out;
+    if (self_route) {
+      dp.self_route = 1;
+      dp.W_g = W_g;
+      dp.b_g = b_g;
+      dp.W_n = W_noise;
+      dp.eps = eps;
+      dp.gate_raw = shape->gates == MOE_GATES_RAW ? 1 : 0;
+      dp.C = C;
+      dp.logits = logits;
+      dp.stats = reinterpret_cast<long long*>(stats);
+      dp.counts = counts;
+      dp.dropped = reinterpret_cast<long long*>(dropped);
+    }
     if ((st = cuda_status(launch_ffn_decode(dp, s))) != MOE_OK) return st;
     // the same kernel did the combine: stage events 3, 4 and 5 all follow it
     if ((st = mark(3)) != MOE_OK) return st;

@@ -26,14 +26,13 @@
 // selected exact logits) are those of the CUDA-core kernels.  Used only when
 // no exact full logit table is asked for (no logits output, no raw-p gates,
 // no expert-choice radii).
-#include "router_rank.cuh"
+#include "router_tc.cuh"
 
 namespace moe {
 namespace {
 
 using namespace router_detail;
 
-constexpr float kFilterMargin = 1.0f / 1024.0f;  // delta = margin * ||x|| * ||w_col||
 
 // Column c of [W_g | W_noise]: bf16 hi / lo parts as row c of wsplit [nc][2d]
 // (hi in k < d, lo in k >= d), the fp32 column as row c of wt [nc][d], and
@@ -82,7 +81,6 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
   const float gam = (n_eff * kU) / (1.0f - n_eff * kU);
   int n_recomputed = 0, n_near = 0;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(p.x);
-  auto wcol = [&](int c, int j) { return __ldg(reinterpret_cast<const float4*>(wt + static_cast<long long>(c) * d + j)); };
 
   const long long nwarps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
   // the approximate logits and the noise of a token, requested one token ahead
@@ -110,136 +108,11 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
   prefetch_row(t + nwarps);
   for (; t < p.T; t += nwarps) {
     prefetch_row(t + 2 * nwarps);
-    const __nv_bfloat16* xrow = x + t * d;
     float ga[SLOTS], za[SLOTS], ep[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) { ga[s] = ga_n[s]; za[s] = za_n[s]; ep[s] = ep_n[s]; }
     load_tok(t + nwarps, ga_n, za_n, ep_n);
-    // ---- token norm
-    float sq = 0.f;
-    for (int j = lane * 4; j < d; j += 128) {
-      float xv[4];
-      Vec4<__nv_bfloat16>::unpack(Vec4<__nv_bfloat16>::load(xrow + j), xv);
-      sq = fmaf(xv[0], xv[0], fmaf(xv[1], xv[1], fmaf(xv[2], xv[2], fmaf(xv[3], xv[3], sq))));
-    }
-    const float nx = sqrtf(warp_sum(sq));
-    // ---- approximate logits and their margins
-    float g[SLOTS], z[SLOTS], xb[SLOTS], lo[SLOTS], up[SLOTS];
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) {
-      const int e = lane + 32 * s;
-      g[s] = z[s] = xb[s] = 0.f;
-      lo[s] = up[s] = -INFINITY;
-      if (e < E) {
-        g[s] = ga[s];
-        float h = g[s] + (p.b_g ? __ldg(p.b_g + e) : 0.f);
-        float dl = kFilterMargin * nx * s_cn[e];
-        if (noisy) {
-          z[s] = za[s];
-          h += ep[s] * softplus_f32(z[s]);
-          dl += fabsf(ep[s]) * kFilterMargin * nx * s_cn[E + e];  // softplus is 1-Lipschitz
-        }
-        dl = dl * 1.25f + 4.f * kU * fabsf(h) + 1e-30f;
-        xb[s] = dl;
-        if (h != h) {  // not a number: let the exact path decide
-          lo[s] = -INFINITY;
-          up[s] = INFINITY;
-        } else {
-          lo[s] = h - dl;
-          up[s] = h + dl;
-        }
-      }
-    }
-    // ---- L = the kr-th largest lower end; candidates reach L with their upper end
-    bool taken[SLOTS];
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) taken[s] = false;
-    float L = -INFINITY;
-    for (int r = 0; r < kr; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int s = 0; s < SLOTS; ++s) {
-        const int e = lane + 32 * s;
-        if (e < E && !taken[s] && better(lo[s], e, bv, be)) { bv = lo[s]; be = e; }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int e2 = __shfl_xor_sync(0xffffffffu, be, o);
-        if (better(v2, e2, bv, be)) { bv = v2; be = e2; }
-      }
-#pragma unroll
-      for (int s = 0; s < SLOTS; ++s)
-        if ((be & 31) == lane && (be >> 5) == s) taken[s] = true;
-      L = bv;
-    }
-    // ---- exact fp32 logits of the candidates, four at a time (warp-uniform)
-    unsigned cm[SLOTS];
-#pragma unroll
-    for (int s = 0; s < SLOTS; ++s) cm[s] = __ballot_sync(0xffffffffu, lane + 32 * s < E && !(up[s] < L));
-    while (true) {
-      int ce[4];
-      int n = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        ce[q] = 0;
-        bool got = false;
-#pragma unroll
-        for (int s = 0; s < SLOTS; ++s) {
-          if (!got && cm[s] != 0u) {
-            ce[q] = (__ffs(cm[s]) - 1) + 32 * s;
-            cm[s] &= cm[s] - 1u;
-            got = true;
-          }
-        }
-        n += got ? 1 : 0;
-      }
-      if (n == 0) break;
-      float ag[4] = {0.f, 0.f, 0.f, 0.f}, az[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int j = lane * 4; j < d; j += 128) {
-        float xv[4];
-        Vec4<__nv_bfloat16>::unpack(Vec4<__nv_bfloat16>::load(xrow + j), xv);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q < n) {
-            const float4 w = wcol(ce[q], j);
-            ag[q] = fmaf(xv[0], w.x, ag[q]);
-            ag[q] = fmaf(xv[1], w.y, ag[q]);
-            ag[q] = fmaf(xv[2], w.z, ag[q]);
-            ag[q] = fmaf(xv[3], w.w, ag[q]);
-            if (noisy) {
-              const float4 u = wcol(E + ce[q], j);
-              az[q] = fmaf(xv[0], u.x, az[q]);
-              az[q] = fmaf(xv[1], u.y, az[q]);
-              az[q] = fmaf(xv[2], u.z, az[q]);
-              az[q] = fmaf(xv[3], u.w, az[q]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < n) {  // warp-uniform
-          ag[q] = warp_sum(ag[q]);
-          if (noisy) az[q] = warp_sum(az[q]);
-        }
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < n) {
-#pragma unroll
-          for (int s = 0; s < SLOTS; ++s) {
-            if (lane == (ce[q] & 31) && s == (ce[q] >> 5)) {
-              g[s] = ag[q];
-              z[s] = az[q];
-              xb[s] = 0.f;  // an exact fp32 contraction: rank_token's own bound covers it
-            }
-          }
-        }
-      }
-    }
-    rank_token<__nv_bfloat16, SLOTS>(p, t, lane, g, z, ep, nx, s_cn, gam, wcol, n_recomputed, n_near, xb);
+    rank_token_filtered<SLOTS>(p, t, lane, ga, za, ep, wt, s_cn, gam, n_recomputed, n_near);
   }
   pdl_trigger();
   if (p.stats != nullptr) {
@@ -268,17 +141,27 @@ size_t router_tc_scratch_bytes(long long T, int d, int E) {
          up(sizeof(float) * nc * d) + up(sizeof(float) * nc);
 }
 
-cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t st) {
-  const int nc = p.W_n ? 2 * p.E : p.E;
+RouterTcScratch router_tc_scratch(void* scratch, long long T, int d, int E) {
   auto up = [](size_t v) { return (v + 255) / 256 * 256; };
   char* base = static_cast<char*>(scratch);
-  float* approx = reinterpret_cast<float*>(base);
-  base += up(sizeof(float) * static_cast<size_t>(p.T) * 2 * p.E);
-  __nv_bfloat16* wsplit = reinterpret_cast<__nv_bfloat16*>(base);
-  base += up(2 * static_cast<size_t>(2 * p.E) * 2 * p.d);
-  float* wt = reinterpret_cast<float*>(base);
-  base += up(sizeof(float) * static_cast<size_t>(2 * p.E) * p.d);
-  float* cn = reinterpret_cast<float*>(base);
+  RouterTcScratch r{};
+  r.approx = reinterpret_cast<float*>(base);
+  base += up(sizeof(float) * static_cast<size_t>(T) * 2 * E);
+  r.wsplit = base;
+  base += up(2 * static_cast<size_t>(2 * E) * 2 * d);
+  r.wt = reinterpret_cast<float*>(base);
+  base += up(sizeof(float) * static_cast<size_t>(2 * E) * d);
+  r.cn = reinterpret_cast<float*>(base);
+  return r;
+}
+
+cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t st) {
+  const int nc = p.W_n ? 2 * p.E : p.E;
+  const RouterTcScratch sc = router_tc_scratch(scratch, p.T, p.d, p.E);
+  float* approx = sc.approx;
+  __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(sc.wsplit);
+  float* wt = sc.wt;
+  float* cn = sc.cn;
   cudaError_t e = launch_pdl(router_tc_prep_kernel, dim3(static_cast<unsigned>(nc)), dim3(256), 0, st, 1, p.W_g,
                              p.W_n, p.d, p.E, wsplit, wt, cn);
   if (e != cudaSuccess) return e;
@@ -298,14 +181,10 @@ cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t 
 // approximate logits g~ [T, nc] written to `approx`.
 cudaError_t launch_router_tc_filter(const RouterParams& p, void* scratch, float* approx, cudaStream_t st) {
   const int nc = p.W_n ? 2 * p.E : p.E;
-  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-  char* base = static_cast<char*>(scratch);
-  base += up(sizeof(float) * static_cast<size_t>(p.T) * 2 * p.E);
-  __nv_bfloat16* wsplit = reinterpret_cast<__nv_bfloat16*>(base);
-  base += up(2 * static_cast<size_t>(2 * p.E) * 2 * p.d);
-  float* wt = reinterpret_cast<float*>(base);
-  base += up(sizeof(float) * static_cast<size_t>(2 * p.E) * p.d);
-  float* cn = reinterpret_cast<float*>(base);
+  const RouterTcScratch sc = router_tc_scratch(scratch, p.T, p.d, p.E);
+  __nv_bfloat16* wsplit = static_cast<__nv_bfloat16*>(sc.wsplit);
+  float* wt = sc.wt;
+  float* cn = sc.cn;
   cudaError_t e = launch_pdl(router_tc_prep_kernel, dim3(static_cast<unsigned>(nc)), dim3(256), 0, st, 1, p.W_g,
                              p.W_n, p.d, p.E, wsplit, wt, cn);
   if (e != cudaSuccess) return e;
