@@ -100,9 +100,9 @@ constexpr int ROUTE_SMEM_WORDS = RED_FLOATS + CNP_FLOATS + 256 /*column norms*/ 
 constexpr int ROUTE_SMEM_BYTES = ROUTE_SMEM_WORDS * 4;
 constexpr int kMaxAssign = 128 * kMaxTopK;           // T * k of a decode-sized batch
 constexpr int kMaxItems = kMaxAssign / EPI_THREADS;  // assignments a dispatch thread holds
-// the dispatch tile's per-(item, warp) expert histogram, the loads and a flag
+// the dispatch tile's per-(item, warp) expert histogram, the loads, a flag, the segment offsets
 __host__ __device__ constexpr int dispatch_words(int Tk, int E) {
-  return ((Tk + EPI_THREADS - 1) / EPI_THREADS) * EPI_WARPS * E + E + 1;
+  return ((Tk + EPI_THREADS - 1) / EPI_THREADS) * EPI_WARPS * E + E + 1 + E + 1;
 }
 
 struct DecodeArgs {
@@ -140,6 +140,7 @@ struct DecodeArgs {
   RouterParams rp;
   int32_t* counts;
   long long* dropped;
+  int32_t* row_of;  // [T, k] grouped row of each assignment (-1: dropped), written by the dispatch tile
 };
 
 __device__ __forceinline__ float gelu_f(float a) { return 0.5f * a * (1.0f + erff(a * 0.70710678118654752f)); }
@@ -172,36 +173,52 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The grouped row of assignment a (-1: dropped or invalid): the dispatch
+// tile's table (self-routed layers), else offsets[idx[a]] + pos[a].
+template <bool kRows>
+__device__ __forceinline__ int grouped_row(const DecodeArgs& g, long long a) {
+  long long row = -1;
+  if (kRows) {
+    row = __ldcg(g.row_of + a);
+  } else {
+    const int ps = __ldcg(g.pos + a);
+    const int e = __ldcg(g.idx + a);
+    if (ps >= 0 && e >= 0 && e < g.E) row = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
+    else if (ps >= 0) row = g.rows;  // an expert id out of range: reported below
+  }
+  if (row >= g.rows) {
+    record_error(g.err, MOE_ERR_BOUNDS);
+    row = -1;
+  }
+  return static_cast<int>(row);  // rows < 2^31 (the workspace's grouped rows)
+}
+
 // The combine of 16 tokens x one 256-column block (the standalone combine's
 // arithmetic, so the layer output is the same bit for bit): per token t and
 // 16-element chunk, acc = fma over the kept ranks r = 0..k-1 of
 // w[t,r] * y[row(t,r)], + the shared experts' output, out = bf16(x + acc),
-// moe_out = acc.  One (token, chunk) item per thread; the loads of every
-// rank are issued before the sums so their latencies overlap.
+// moe_out = acc.  One (token, chunk) item per thread.  It runs once per CTA
+// at the end of the kernel, from a cold instruction cache, so the code is
+// kept short: the first KF ranks' rows and gates are requested together,
+// their y chunks KB ranks at a time; ranks past KF (k > 8) one by one.
 constexpr int COMBINE_TOKENS = 16;
+template <bool kRows>
 __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg, int item) {
   const int t = tg * COMBINE_TOKENS + item / (BN / 16);
   const int c = cb * BN + (item % (BN / 16)) * 16;
   if (t >= g.T || c >= g.d) return;
   const long long base = static_cast<long long>(t) * g.d + c;
-  long long row[kMaxTopK];
-  float wt[kMaxTopK];
+  const long long a0 = static_cast<long long>(t) * g.k;
+  constexpr int KF = 8, KB = 2;
+  int row[KF];
+  float wt[KF];
 #pragma unroll
-  for (int r = 0; r < kMaxTopK; ++r) {
+  for (int r = 0; r < KF; ++r) {
     row[r] = -1;
     wt[r] = 0.f;
     if (r < g.k) {
-      const long long a = static_cast<long long>(t) * g.k + r;
-      const int ps = __ldcg(g.pos + a);
-      const int e = __ldcg(g.idx + a);
-      wt[r] = __ldcg(g.w + a);
-      if (ps >= 0) {  // dropped: the residual carries the token
-        if (e >= 0 && e < g.E) row[r] = static_cast<long long>(__ldcg(g.offsets + e)) + ps;
-        if (row[r] < 0 || row[r] >= g.rows) {
-          record_error(g.err, MOE_ERR_BOUNDS);
-          row[r] = -1;
-        }
-      }
+      wt[r] = __ldcg(g.w + a0 + r);
+      row[r] = grouped_row<kRows>(g, a0 + r);
     }
   }
   float rv[16];
@@ -218,19 +235,40 @@ __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-#pragma unroll 4
-  for (int r = 0; r < g.k; ++r) {
-    if (row[r] < 0) continue;
-    const float4* ysrc = reinterpret_cast<const float4*>(g.y + row[r] * g.d + c);
-    float4 v[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) v[q] = __ldcg(ysrc + q);
+  auto add_rank = [&](const float4 (&v)[4], float w) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      acc[4 * q] = fmaf(wt[r], v[q].x, acc[4 * q]);
-      acc[4 * q + 1] = fmaf(wt[r], v[q].y, acc[4 * q + 1]);
-      acc[4 * q + 2] = fmaf(wt[r], v[q].z, acc[4 * q + 2]);
-      acc[4 * q + 3] = fmaf(wt[r], v[q].w, acc[4 * q + 3]);
+      acc[4 * q] = fmaf(w, v[q].x, acc[4 * q]);
+      acc[4 * q + 1] = fmaf(w, v[q].y, acc[4 * q + 1]);
+      acc[4 * q + 2] = fmaf(w, v[q].z, acc[4 * q + 2]);
+      acc[4 * q + 3] = fmaf(w, v[q].w, acc[4 * q + 3]);
+    }
+  };
+#pragma unroll
+  for (int r0 = 0; r0 < KF; r0 += KB) {
+    float4 v[KB][4];
+#pragma unroll
+    for (int r = 0; r < KB; ++r) {
+      if (row[r0 + r] >= 0) {
+        const float4* ysrc = reinterpret_cast<const float4*>(g.y + static_cast<long long>(row[r0 + r]) * g.d + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[r][q] = __ldcg(ysrc + q);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < KB; ++r)
+      if (row[r0 + r] >= 0) add_rank(v[r], wt[r0 + r]);
+  }
+#pragma unroll 1
+  for (int r = KF; r < g.k; ++r) {
+    const long long rw = grouped_row<kRows>(g, a0 + r);  // widened for the address
+    const float w = __ldcg(g.w + a0 + r);
+    if (rw >= 0) {
+      const float4* ysrc = reinterpret_cast<const float4*>(g.y + rw * g.d + c);
+      float4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = __ldcg(ysrc + q);
+      add_rank(v, w);
     }
   }
   if (g.y_shared) {
@@ -501,6 +539,7 @@ __device__ __forceinline__ bool dispatch_tile(const DecodeArgs& g, int et, const
   int* hist = sbuf;                      // [U][EPI_WARPS][E]
   int* s_tot = hist + U * EPI_WARPS * E;  // [E] loads
   int* s_ok = s_tot + E;
+  int* s_off = s_ok + 1;                  // [E+1] segment offsets
   for (int i = et; i < U * EPI_WARPS * E; i += EPI_THREADS) sts_s32(hist + i, 0);
   // thread 0 waits for the rank tiles; its result reaches the others through
   // shared memory (written before the barrier, read after it)
@@ -553,6 +592,7 @@ __device__ __forceinline__ bool dispatch_tile(const DecodeArgs& g, int et, const
         record_error(g.err, MOE_ERR_BOUNDS);  // the rank tiles write no such id
       }
       g.pos[t * k + r] = ps;
+      rk[u] = ps;  // kept for the grouped rows below
     }
   }
   if (wr == 0) {
@@ -579,6 +619,7 @@ __device__ __forceinline__ bool dispatch_tile(const DecodeArgs& g, int et, const
       if (ex < E) {
         g.counts[ex] = v[q];
         g.offsets[ex] = off;
+        sts_s32(s_off + ex, off);
       }
       off += v[q];
     }
@@ -586,6 +627,16 @@ __device__ __forceinline__ bool dispatch_tile(const DecodeArgs& g, int et, const
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) drop += __shfl_xor_sync(0xffffffffu, drop, o);
     if (lane == 0) *g.dropped = drop;
+  }
+  if (!eb.sync()) return false;
+  // the grouped row of every assignment (-1: dropped), which the combine reads
+#pragma unroll
+  for (int u = 0; u < kMaxItems; ++u) {
+    const int j2 = u * EPI_THREADS + et;
+    if (u < U && j2 < Tk) {
+      const int r = j2 / T, t = j2 - r * T;
+      g.row_of[t * k + r] = rk[u] >= 0 ? lds_s32(s_off + ev[u]) + rk[u] : -1;
+    }
   }
   __threadfence();
   return eb.sync();
@@ -909,7 +960,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ready) break;
         (void)ld_acquire(done2 + cb);  // every lane's reads below follow the completed count
         static_assert(COMBINE_TOKENS * (BN / 16) == EPI_WARPS * 32, "one combine item per epilogue thread");
-        combine_item(g, cb, tg, (warp - 4) * 32 + lane);
+        combine_item<kRoute>(g, cb, tg, (warp - 4) * 32 + lane);
         continue;
       }
       const bool p1 = id < total1;
@@ -1210,6 +1261,7 @@ cudaError_t launch_ffn_decode(const DecodeFfnParams& p, cudaStream_t st) {
     g.C = p.C;
     g.counts = p.counts;
     g.dropped = p.dropped;
+    g.row_of = p.row_of;
     RouterParams& rp = g.rp;
     rp.x = p.x;
     rp.W_g = p.W_g;

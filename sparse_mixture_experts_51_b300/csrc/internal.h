@@ -269,6 +269,7 @@ struct DecodeFfnParams {
   long long* stats;        // router counters or null
   int32_t* counts;         // [E]
   long long* dropped;      // [1]
+  int32_t* row_of;         // [T,k] workspace: grouped row of each assignment, -1 if dropped
 };
 bool ffn_decode_applies(const moe_shape_t& s);
 // the fused kernel can also route the batch: overflow drop, nc = E (2E with the

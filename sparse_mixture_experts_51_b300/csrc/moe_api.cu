@@ -698,6 +698,7 @@ static moe_status_t forward_impl(const moe_shape_t* shape, double capacity_facto
       dp.stats = reinterpret_cast<long long*>(stats);
       dp.counts = counts;
       dp.dropped = reinterpret_cast<long long*>(dropped);
+      dp.row_of = at<int32_t>(ws, L.row_of);
     }
     if ((st = cuda_status(launch_ffn_decode(dp, s))) != MOE_OK) return st;
     // the same kernel did the combine: stage events 3, 4 and 5 all follow it
