@@ -58,11 +58,10 @@ SINGLE_THREAD_CPU = ("tiny_fp32", "bf16_t4096", "decode_t128")
 HBM_NOMINAL_GBS = 8000.0
 
 # DRAM traffic of the dominant kernel per launch, from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and by the
-# hash of the kernel sources it was taken on; a changed kernel reports null.
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload; each
+# record lists the kernel sources it was taken on and their hash, and a
+# record whose sources have changed since reports null.
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-GEMM_SOURCES = ["sparse_mixture_experts_51_b300/csrc/gemm_tc.cu", "sparse_mixture_experts_51_b300/csrc/ffn_decode.cu",
-                "sparse_mixture_experts_51_b300/csrc/common.cuh"]
 
 
 def parse_args(argv=None):
@@ -81,9 +80,9 @@ def parse_args(argv=None):
 
 # ---------------------------------------------------------------- helpers
 
-def kernel_hash() -> str:
+def kernel_hash(sources) -> str:
     h = hashlib.sha256()
-    for f in GEMM_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -146,7 +145,7 @@ def recorded_traffic(name):
         return None
     with open(TRAFFIC_FILE) as fh:
         rec = json.load(fh).get(name)
-    if rec and rec.get("kernel_hash") == kernel_hash():
+    if rec and rec.get("sources") and rec.get("kernel_hash") == kernel_hash(rec["sources"]):
         return rec.get("dram_bytes_per_launch")
     return None
 
