@@ -11,6 +11,9 @@ namespace moe {
 namespace router_detail {
 
 constexpr float kU = 5.9604644775390625e-8f;  // unit roundoff of fp32, 2^-24
+// a token is counted as a near tie when its k-th and (k+1)-th fp32 logits
+// are closer than this (a diagnostic; the selection is exact either way)
+constexpr float kNearTie = 1e-4f;
 
 template <typename TX>
 struct Vec16;
@@ -258,7 +261,7 @@ __device__ __forceinline__ void rank_token(const RouterParams& p, long long t, i
   bool safe = true, near = false;
   if (lane < kr) {
     safe = lo > below && lo > -INFINITY && my_b < INFINITY;
-    if (lane == k - 1 && k < E) near = my_h - (kr > k ? h_k : restH) < 1e-4f;
+    if (lane == k - 1 && k < E) near = my_h - (kr > k ? h_k : restH) < kNearTie;
   }
   if (__any_sync(0xffffffffu, near)) ++n_near;
   const unsigned unsafe = __ballot_sync(0xffffffffu, !safe) & ((1u << kr) - 1u);

@@ -1,5 +1,5 @@
-// The per-token step of the tensor-core router filter (router_tc.cu), shared
-// with the fused decode kernel (ffn_decode.cu): one warp takes token t's
+// The per-token step of the tensor-core router filter (router_tc.cu): one
+// warp takes token t's
 // approximate logits g~ (from the filter GEMM of x against the bf16 hi + lo
 // split of the router weights), bounds each one by the filter margin, finds
 // the experts that may still hold one of the top ranks, recomputes those
@@ -91,10 +91,45 @@ __device__ __forceinline__ void rank_token_filtered(const RouterParams& p, long 
       if ((be & 31) == lane && (be >> 5) == s) taken[s] = true;
     L = bv;
   }
-  // ---- exact fp32 logits of the candidates, four at a time (warp-uniform)
   unsigned cm[SLOTS];
 #pragma unroll
   for (int s = 0; s < SLOTS; ++s) cm[s] = __ballot_sync(0xffffffffu, lane + 32 * s < E && !(up[s] < L));
+  // ---- top-1 without a backup rank, a single candidate: the bounds alone
+  // prove it is the top expert (its lower end L is above every other upper
+  // end), and its gate, the softmax over the one selected logit, is exactly
+  // 1 -- what rank_token writes after the recomputation below.  The token is
+  // written at once, unless the bounds leave room for a near tie (top minus
+  // the best other fp32 logit below kNearTie: that counter needs the values).
+  if (k == 1 && kr == 1) {
+    int ncand = 0;
+#pragma unroll
+    for (int s = 0; s < SLOTS; ++s) ncand += __popc(cm[s]);
+    if (ncand == 1) {
+      float other_up = -INFINITY;
+      int win = -1;
+#pragma unroll
+      for (int s = 0; s < SLOTS; ++s) {
+        const int e = lane + 32 * s;
+        if (e < E) {
+          if ((cm[s] >> lane) & 1u) win = e;
+          else other_up = fmaxf(other_up, up[s]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        other_up = fmaxf(other_up, __shfl_xor_sync(0xffffffffu, other_up, o));
+        win = max(win, __shfl_xor_sync(0xffffffffu, win, o));
+      }
+      if (L - other_up >= 2.0f * kNearTie) {  // false for any NaN or infinity
+        if (lane == 0) {
+          p.idx[t] = win;
+          p.w[t] = 1.0f;
+        }
+        return;
+      }
+    }
+  }
+  // ---- exact fp32 logits of the candidates, four at a time (warp-uniform)
   while (true) {
     int ce[4];
     int n = 0;

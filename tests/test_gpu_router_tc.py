@@ -53,10 +53,12 @@ def test_tensor_core_router_with_rerouting():
     check_layer(w, inp, gpu, ref)
 
 
-def test_tensor_core_router_exact_ties():
+@pytest.mark.parametrize("k", [1, 2])
+def test_tensor_core_router_exact_ties(k):
     """Integer tokens and router weights: many exactly equal logits; the
-    lower expert index wins through the filter path too."""
-    w = W.Workload("tc_ties", T=16384, d=64, E=32, k=2, F=64, act=W.ACT_GELU, capacity_factor=2.0,
+    lower expert index wins through the filter path too (top-1: tied experts
+    are both candidates, so the single-candidate shortcut never takes them)."""
+    w = W.Workload("tc_ties", T=16384, d=64, E=32, k=k, F=64, act=W.ACT_GELU, capacity_factor=2.0,
                    dtype=torch.bfloat16, seed=85)
     inp = W.make_inputs(w)
     g = torch.Generator().manual_seed(86)
