@@ -201,13 +201,16 @@ __device__ __forceinline__ int grouped_row(const DecodeArgs& g, long long a) {
 // at the end of the kernel, from a cold instruction cache, so the code is
 // kept short: the first KF ranks' rows and gates are requested together,
 // their y chunks KB ranks at a time; ranks past KF (k > 8) one by one.
+// Everything but the y rows is fetched before `wait` (warp-collective,
+// called by every lane; false: give up) returns, so a combine tile taken
+// early does that part while its column block's rows are still being stored.
 constexpr int COMBINE_TOKENS = 16;
-template <bool kRows>
-__device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg, int item) {
+template <bool kRows, typename Wait>
+__device__ __forceinline__ bool combine_item(const DecodeArgs& g, int cb, int tg, int item, Wait wait) {
   const int t = tg * COMBINE_TOKENS + item / (BN / 16);
   const int c = cb * BN + (item % (BN / 16)) * 16;
-  if (t >= g.T || c >= g.d) return;
-  const long long base = static_cast<long long>(t) * g.d + c;
+  const bool valid = t < g.T && c < g.d;
+  const long long base = valid ? static_cast<long long>(t) * g.d + c : 0;
   const long long a0 = static_cast<long long>(t) * g.k;
   constexpr int KF = 8, KB = 2;
   int row[KF];
@@ -216,13 +219,14 @@ __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg
   for (int r = 0; r < KF; ++r) {
     row[r] = -1;
     wt[r] = 0.f;
-    if (r < g.k) {
+    if (valid && r < g.k) {
       wt[r] = __ldcg(g.w + a0 + r);
       row[r] = grouped_row<kRows>(g, a0 + r);
     }
   }
   float rv[16];
-  {
+  float ys[16];
+  if (valid) {
     const uint4* src = reinterpret_cast<const uint4*>(g.x_res + base);
     const uint4 a = __ldcg(src), b = __ldcg(src + 1);
     const uint32_t u[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
@@ -232,6 +236,21 @@ __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg
       rv[2 * i + 1] = __uint_as_float(u[i] & 0xffff0000u);
     }
   }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ys[i] = 0.f;
+  if (valid && g.y_shared) {
+    const float4* ssrc = reinterpret_cast<const float4*>(g.y_shared + base);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = __ldcg(ssrc + q);
+      ys[4 * q] = v.x;
+      ys[4 * q + 1] = v.y;
+      ys[4 * q + 2] = v.z;
+      ys[4 * q + 3] = v.w;
+    }
+  }
+  if (!wait()) return false;
+  if (!valid) return true;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -272,15 +291,8 @@ __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg
     }
   }
   if (g.y_shared) {
-    const float4* ssrc = reinterpret_cast<const float4*>(g.y_shared + base);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = __ldcg(ssrc + q);
-      acc[4 * q] += v.x;
-      acc[4 * q + 1] += v.y;
-      acc[4 * q + 2] += v.z;
-      acc[4 * q + 3] += v.w;
-    }
+    for (int i = 0; i < 16; ++i) acc[i] += ys[i];
   }
   if (g.moe_out) {
     float4* mo = reinterpret_cast<float4*>(g.moe_out + base);
@@ -296,6 +308,7 @@ __device__ __forceinline__ void combine_item(const DecodeArgs& g, int cb, int tg
   uint4* dst = reinterpret_cast<uint4*>(g.out + base);
   dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  return true;
 }
 
 // ---------------------------------------------------------------- routing tiles
@@ -954,13 +967,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int e2 = lane; e2 < E; e2 += 32) n_active += __ldcg(g.offsets + e2 + 1) > __ldcg(g.offsets + e2) ? 1 : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) n_active += __shfl_xor_sync(0xffffffffu, n_active, o);
-        bool ready = true;
-        if (lane == 0) ready = wait_flag(done2 + cb, EPI_WARPS * n_active, g.err, abort_flag);
-        ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
-        if (!ready) break;
-        (void)ld_acquire(done2 + cb);  // every lane's reads below follow the completed count
+        auto block_stored = [&]() -> bool {
+          bool ready = true;
+          if (lane == 0) ready = wait_flag(done2 + cb, EPI_WARPS * n_active, g.err, abort_flag);
+          ready = __shfl_sync(0xffffffffu, ready ? 1 : 0, 0) != 0;
+          if (ready) (void)ld_acquire(done2 + cb);  // every lane's reads of y follow the completed count
+          return ready;
+        };
         static_assert(COMBINE_TOKENS * (BN / 16) == EPI_WARPS * 32, "one combine item per epilogue thread");
-        combine_item<kRoute>(g, cb, tg, (warp - 4) * 32 + lane);
+        if (!combine_item<kRoute>(g, cb, tg, (warp - 4) * 32 + lane, block_stored)) break;
         continue;
       }
       const bool p1 = id < total1;
