@@ -45,24 +45,28 @@
 //
 // Tiles are claimed one at a time from a ticket in the workspace: the
 // routing tiles (self-routed layers), every phase-1 tile, then every
-// phase-2 tile (experts in order), then the combine tiles.  A phase-2 tile of expert e waits until all phase-1 tiles
-// of e have stored their rows, and a combine tile until every active
-// expert's phase-2 tile of its column block has (counts of finished
-// epilogue warps).  Every tile a CTA waits on was claimed earlier by a CTA
-// that is running and does not wait on anything later, so the waits always
-// end.  The routing tables (idx, pos, offsets, w) are read only after
-// griddepcontrol.wait, or (self-routed) once the dispatch tile has
-// published them; a phase-2 tile of an expert without kept rows is
-// skipped.  A CTA that claims a routing tile claims nothing more until its
-// epilogue warps have run it, so the routing tiles spread over CTAs.  The last CTA to finish clears the ticket and counts for the
-// next call.
+// phase-2 tile (experts in order), then the combine tiles.  A phase-2 tile
+// of expert e waits until all phase-1 tiles of e have stored their rows,
+// and a combine tile until every active expert's phase-2 tile of its column
+// block has (counts of finished epilogue warps); a combine tile fetches
+// everything but those rows before it waits.  Every tile a CTA waits on was
+// claimed earlier by a CTA that is running and does not wait on anything
+// later, so the waits always end.  The routing tables (idx, pos, offsets,
+// w) are read only after griddepcontrol.wait, or (self-routed) once the
+// dispatch tile has published them; phase 1 of a self-routed layer does not
+// wait for them (until they are published it stores every token's hidden
+// row); a phase-2 tile of an expert without kept rows is skipped.  A CTA
+// that claims a routing tile claims nothing more until its epilogue warps
+// have run it, so the routing tiles spread over CTAs.  The last CTA to
+// finish clears the ticket and counts for the next call.
 //
 // Roles per CTA (384 threads): warp 0 claims tiles and issues TMA loads
 // (4-stage ring of 48 KB: A 128x64, B 256x64, 128-byte swizzle); warp 1
 // issues tcgen05.mma (M=128, N=256, K=16) into one of two TMEM accumulators;
 // warp 2 owns TMEM; warps 4-11 drain the accumulator (two per TMEM lane
 // quarter, half of the 32-column chunks each) with whole-sector stores, and
-// run the combine tiles (one (token, 16-column chunk) item per thread).
+// run the routing tiles and the combine tiles (one (token, 16-column
+// chunk) item per thread).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
