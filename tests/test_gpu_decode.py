@@ -41,6 +41,10 @@ CASES = [
     # the widest logit table the rank tiles take: 128 experts with the noise projection (256 columns)
     W.Workload("dec_e128_noisy", T=128, d=256, E=128, k=4, F=128, act=W.ACT_SWIGLU, capacity_factor=1.5,
                dtype=torch.bfloat16, seed=88, noisy=True),
+    # the smallest self-routed layer: 4 experts, top-4 (every token takes every expert), two rank
+    # tiles the second of which holds one token, logit columns split 256 ways along d
+    W.Workload("dec_tiny", T=5, d=64, E=4, k=4, F=64, act=W.ACT_SWIGLU, capacity_factor=1.0,
+               dtype=torch.bfloat16, seed=90),
     # E = 48: not a power of two, so the router and the dispatch run as their own kernels
     W.Workload("dec_e48", T=96, d=256, E=48, k=4, F=256, act=W.ACT_SWIGLU, capacity_factor=1.25,
                dtype=torch.bfloat16, seed=89),
