@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(256) router_tc_prep_kernel(const float* W_g, c
 }
 
 template <int SLOTS>
-__global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, const float* approx, const float* wt,
+__global__ void __launch_bounds__(256, 2) router_tc_rank_kernel(RouterParams p, const float* approx, const float* wt,
                                                              const float* cn_g) {
   __shared__ float s_cn[2 * kMaxExperts];
   const int lane = threadIdx.x & 31;
@@ -106,13 +106,38 @@ __global__ void __launch_bounds__(256, 3) router_tc_rank_kernel(RouterParams p, 
   };
   prefetch_row(t);
   prefetch_row(t + nwarps);
+  // d <= 1024: the next token's row is held in registers (8 loads a lane) so
+  // its norm never waits on memory; longer rows are read in the step itself
+  constexpr int XR = 8;
+  const bool xreg = d <= XR * 128;
+  typename Vec4<__nv_bfloat16>::raw xr_n[XR];
+  auto load_row = [&](long long tt) {
+#pragma unroll
+    for (int i = 0; i < XR; ++i) {
+      const int j = i * 128 + lane * 4;
+      xr_n[i] = (xreg && tt < p.T && j < d) ? Vec4<__nv_bfloat16>::load(x + tt * d + j) : Vec4<__nv_bfloat16>::zero();
+    }
+  };
+  load_row(t);
   for (; t < p.T; t += nwarps) {
     prefetch_row(t + 2 * nwarps);
     float ga[SLOTS], za[SLOTS], ep[SLOTS];
 #pragma unroll
     for (int s = 0; s < SLOTS; ++s) { ga[s] = ga_n[s]; za[s] = za_n[s]; ep[s] = ep_n[s]; }
     load_tok(t + nwarps, ga_n, za_n, ep_n);
-    rank_token_filtered<SLOTS>(p, t, lane, ga, za, ep, wt, s_cn, gam, n_recomputed, n_near);
+    float nx = -1.f;
+    if (xreg) {
+      float sq = 0.f;
+#pragma unroll
+      for (int i = 0; i < XR; ++i) {
+        float xv[4];
+        Vec4<__nv_bfloat16>::unpack(xr_n[i], xv);
+        sq = fmaf(xv[0], xv[0], fmaf(xv[1], xv[1], fmaf(xv[2], xv[2], fmaf(xv[3], xv[3], sq))));
+      }
+      nx = sqrtf(warp_sum(sq));
+      load_row(t + nwarps);
+    }
+    rank_token_filtered<SLOTS>(p, t, lane, ga, za, ep, wt, s_cn, gam, n_recomputed, n_near, nx);
   }
   pdl_trigger();
   if (p.stats != nullptr) {
@@ -169,9 +194,10 @@ cudaError_t launch_router_tc(const RouterParams& p, void* scratch, cudaStream_t 
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  // persistent: three 8-warp blocks per SM (80 registers a thread), warps stride the tokens
+  // persistent: two 8-warp blocks per SM (up to 128 registers a thread: each
+  // warp holds its next token's row), warps stride the tokens
   const long long want = (static_cast<long long>(p.T) + 7) / 8;
-  const unsigned grid = static_cast<unsigned>(want < 3LL * sms ? want : 3LL * sms);
+  const unsigned grid = static_cast<unsigned>(want < 2LL * sms ? want : 2LL * sms);
   if (p.E <= 32) return launch_pdl(router_tc_rank_kernel<1>, dim3(grid), dim3(256), 0, st, 1, p, approx, wt, cn);
   if (p.E <= 64) return launch_pdl(router_tc_rank_kernel<2>, dim3(grid), dim3(256), 0, st, 1, p, approx, wt, cn);
   return launch_pdl(router_tc_rank_kernel<4>, dim3(grid), dim3(256), 0, st, 1, p, approx, wt, cn);

@@ -22,24 +22,28 @@ constexpr float kFilterMargin = 1.0f / 1024.0f;
 // error factor of the exact recomputation (summation depth d/32 + 5).
 // ga/za/ep: this token's approximate gate and noise logits and its noise
 // draws (lane e + 32 s holds expert e), loaded by the caller.
+// nx_in: the token's norm when the caller has it (< 0: computed here).
 template <int SLOTS>
 __device__ __forceinline__ void rank_token_filtered(const RouterParams& p, long long t, int lane,
                                                     const float (&ga)[SLOTS], const float (&za)[SLOTS],
                                                     const float (&ep)[SLOTS], const float* wt, const float* cn,
-                                                    float gam, int& n_recomputed, int& n_near) {
+                                                    float gam, int& n_recomputed, int& n_near, float nx_in = -1.f) {
   const int E = p.E, d = p.d, k = p.k;
   const bool noisy = p.W_n != nullptr;
   const int kr = (p.backup != nullptr && k < E) ? k + 1 : k;
   const __nv_bfloat16* xrow = static_cast<const __nv_bfloat16*>(p.x) + t * d;
   auto wcol = [&](int c, int j) { return __ldg(reinterpret_cast<const float4*>(wt + static_cast<long long>(c) * d + j)); };
   // ---- token norm
-  float sq = 0.f;
-  for (int j = lane * 4; j < d; j += 128) {
-    float xv[4];
-    Vec4<__nv_bfloat16>::unpack(Vec4<__nv_bfloat16>::load(xrow + j), xv);
-    sq = fmaf(xv[0], xv[0], fmaf(xv[1], xv[1], fmaf(xv[2], xv[2], fmaf(xv[3], xv[3], sq))));
+  float nx = nx_in;
+  if (nx < 0.f) {
+    float sq = 0.f;
+    for (int j = lane * 4; j < d; j += 128) {
+      float xv[4];
+      Vec4<__nv_bfloat16>::unpack(Vec4<__nv_bfloat16>::load(xrow + j), xv);
+      sq = fmaf(xv[0], xv[0], fmaf(xv[1], xv[1], fmaf(xv[2], xv[2], fmaf(xv[3], xv[3], sq))));
+    }
+    nx = sqrtf(warp_sum(sq));
   }
-  const float nx = sqrtf(warp_sum(sq));
   // ---- approximate logits and their margins
   float g[SLOTS], z[SLOTS], xb[SLOTS], lo[SLOTS], up[SLOTS];
 #pragma unroll
