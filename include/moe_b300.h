@@ -316,6 +316,16 @@ MOE_API moe_status_t moe_combine(const moe_shape_t* shape, int32_t C, const floa
  * ranks the remaining candidates exactly as moe_route does; the margin
  * assumes the tensor core's fp32 accumulation of exact bf16 products loses
  * fewer than about ten of fp32's 24 bits per step.
+ * Decode-sized bf16 batches (T <= 128 with T*k >= 4E, d and d_ff multiples
+ * of 64) run both expert GEMMs and the combine in one kernel.
+ * - Self-routing: when the overflow policy is drop and the logit table has a
+ *   power-of-two number of columns from 4 to 256, that kernel also routes
+ *   and dispatches the batch, so the whole layer is one launch.
+ * - Same results: its top-k, slots and drops are exactly moe_route's and
+ *   moe_dispatch's.
+ * - Rounding: its fp32 logits are summed in another order, so logits and w
+ *   may differ from moe_route's in the last bits (within the same rigorous
+ *   bound).
  * With overflow re-routing (shape->overflow) idx holds, for each
  * assignment, the expert it was finally sent to (the backup for a re-routed
  * one), pos its slot there, dropped the assignments left without an expert.
